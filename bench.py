@@ -1,0 +1,404 @@
+"""Benchmark of the fused attention forward on GB300.
+
+One step = one pass of the whole hot path on synthetic inputs already resident in device memory:
+  * prefill: B=8, Hq=8, Hkv=2, S=8192, D=128, bf16, causal (long-context throughput workload);
+  * decode:  B=32, Hq=8, Hkv=2, D=128, bf16 cache, per-sequence lengths uniform in [256, 4096].
+The L2 cache is flushed (a 512 MiB memset) before each timed kernel region, outside the events.
+
+Printed (rank 0, one JSON line): ``value`` = prefill TFLOP/s (algorithmic causal flops over the
+measured prefill time), the decode GB/s (algorithmic bytes: every valid K/V row once, q and o)
+under ``decode``, the roofline fractions against the measured peaks, an end-to-end figure through
+the public API with host buffers (copies inside the timed region), SM clocks sampled during the
+timed region, and the fp64 CPU oracle timed on a bounded sample of the same workload.
+
+``--impl reference`` times that oracle alone (the only reference that exists for this method) on
+the host cores, on the same workload and metric.
+
+Multi-GPU: run under torchrun; every rank runs the same workload independently (replicas, weak
+scaling); the slowest rank's time is used and ``value`` is the sum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+PREFILL = workloads.CONFIGS["c5b"]
+DECODE = workloads.CONFIGS["c4b"]
+METRIC = "prefill attention TFLOP/s and decode KV-read GB/s, % of GB300 roofline"
+FLUSH_BYTES = 512 << 20
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="target CPU time of the oracle sample")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# --------------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.index), "-lms", "200"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- distributed
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int, dev) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- oracle sample
+
+
+def oracle_sample(seconds: float):
+    """Time the fp64 oracle on a bounded sample of the bench workload. Returns dict with the
+    prefill TFLOP/s and decode GB/s the oracle reaches on its sample, cores and a description."""
+    import oracle
+
+    lib = oracle.load()
+    cores = oracle.num_threads(lib)
+    cfg = PREFILL
+    q, k, v = workloads.config_prefill_inputs(cfg)
+    # rows spread over the causal range, (b, h) cycling; work per row = (i + 1) keys
+    rng = np.random.default_rng(0)
+    n_rows = 256
+    rows = []
+    t_pref = 0.0
+    flops = 0
+    done = 0
+    while True:
+        b = rng.integers(0, cfg.B, n_rows)
+        h = rng.integers(0, cfg.Hq, n_rows)
+        i = rng.integers(0, cfg.S, n_rows)
+        rows = ((b * cfg.Hq + h) * cfg.S + i).astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.prefill(q, k, v, True, cfg.scale, rows=rows, lib=lib)
+        t_pref += time.perf_counter() - t0
+        flops += int(np.sum(4 * cfg.D * (i + 1)))
+        done += n_rows
+        if t_pref > 0.7 * seconds:
+            break
+    dq, dkc, dvc, sl = workloads.config_decode_inputs(DECODE)
+    t_dec = 0.0
+    reps = 0
+    while True:
+        t0 = time.perf_counter()
+        oracle.decode(dq, dkc, dvc, sl, DECODE.scale, lib=lib)
+        t_dec += time.perf_counter() - t0
+        reps += 1
+        if t_dec > 0.3 * seconds:
+            break
+    dec_bytes = workloads.decode_bytes(sl.tolist(), DECODE.Hq, DECODE.Hkv, DECODE.D)
+    return {
+        "prefill_tflops": flops / t_pref / 1e12,
+        "decode_gbs": dec_bytes * reps / t_dec / 1e9,
+        "cores": cores,
+        "sample": (f"prefill: {done} query rows of the B8 S8192 causal workload drawn uniformly "
+                   f"over (b, h, i), {t_pref:.1f} s; decode: {reps} full B32 step(s), "
+                   f"{t_dec:.1f} s; fp64, OpenMP over rows"),
+        "seconds": t_pref + t_dec,
+    }
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if world > 1 and rank != 0:
+        return
+    steps, warmup = args.steps, args.warmup
+    per = max(1.0, 120.0 / max(1, steps + warmup))  # whole run within a few minutes
+    per = min(per, 10.0)
+    for _ in range(warmup):
+        oracle_sample(min(per, 2.0))
+    vals, dvals, cores, sample = [], [], None, None
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        r = oracle_sample(per)
+        vals.append(r["prefill_tflops"])
+        dvals.append(r["decode_gbs"])
+        cores, sample = r["cores"], r["sample"]
+    wall = time.perf_counter() - t0
+    v = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": steps, "warmup": warmup,
+        "ms_per_step": wall / steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_block(),
+        "decode": {"value": statistics.median(dvals), "unit": "GB/s"},
+        "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_block():
+    return {
+        "workload": ("prefill B8 S8192 Hq8 Hkv2 D128 bf16 causal + decode B32 Hq8 Hkv2 D128 "
+                     "bf16 cache, lengths U[256,4096] (seed 0)"),
+        "prefill": {"B": PREFILL.B, "S": PREFILL.S, "Hq": PREFILL.Hq, "Hkv": PREFILL.Hkv,
+                    "D": PREFILL.D, "causal": True},
+        "decode": {"B": DECODE.B, "Hq": DECODE.Hq, "Hkv": DECODE.Hkv, "D": DECODE.D,
+                   "max_len": DECODE.max_len, "lengths": "uniform [256, 4096]"},
+        "l2": "flushed (512 MiB memset) before every timed kernel region",
+        "parallelism": "replicas",
+    }
+
+
+# --------------------------------------------------------------------------- our kernels
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.distributed.init_process_group(backend="nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    from causal_gqa_attention_gb300 import build as cbuild
+
+    cbuild.build()
+    import causal_gqa_attention_gb300 as cga
+
+    cga.load_library()
+    pk = peaks()
+
+    # inputs resident on the device
+    q, k, v = [t.to(dev) for t in workloads.config_prefill_inputs(PREFILL)]
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    dq, dkc, dvc, dsl = workloads.config_decode_inputs(DECODE, nan_fill=False)
+    dec_bytes = workloads.decode_bytes(dsl.tolist(), DECODE.Hq, DECODE.Hkv, DECODE.D)
+    dq, dkc, dvc, dsl = dq.to(dev), dkc.to(dev), dvc.to(dev), dsl.to(dev)
+    do = torch.empty_like(dq)
+    cga.attn_reserve_workspace(DECODE.B, DECODE.Hq, DECODE.Hkv, DECODE.D, DECODE.max_len)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    pflops = workloads.prefill_flops(PREFILL.B, PREFILL.Hq, PREFILL.S, PREFILL.D, True)
+    stream = torch.cuda.current_stream(dev)
+
+    def run_prefill():
+        cga.prefill(q, k, v, causal=True, out=o, lse=lse, return_lse=True)
+
+    def run_decode():
+        cga.decode(dq, dkc, dvc, dsl, out=do)
+
+    for _ in range(args.warmup):
+        run_prefill()
+        run_decode()
+    torch.cuda.synchronize()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for s in range(args.steps):
+        flush.zero_()
+        ev[s][0].record(stream)
+        run_prefill()
+        ev[s][1].record(stream)
+        flush.zero_()
+        ev[s][2].record(stream)
+        run_decode()
+        ev[s][3].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t_wall = time.perf_counter() - t_wall
+    clocks = sampler.stop()
+    assert cga.device_status() == 0, "device status word set during the bench"
+
+    pre_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.steps)]
+    dec_ms = [ev[s][2].elapsed_time(ev[s][3]) for s in range(args.steps)]
+    pre_mean = max_over_ranks(sum(pre_ms) / len(pre_ms), world, dev)
+    dec_mean = max_over_ranks(sum(dec_ms) / len(dec_ms), world, dev)
+    step_ms = pre_mean + dec_mean
+    tflops = pflops / (pre_mean * 1e-3) / 1e12
+    dec_gbs = dec_bytes / (dec_mean * 1e-3) / 1e9
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = [t.cpu().pin_memory() for t in (q, k, v)]
+        ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        hdq, hdk, hdv, hdsl = [t.cpu().pin_memory() for t in (dq, dkc, dvc, dsl)]
+        hdo = torch.empty(do.shape, dtype=do.dtype).pin_memory()
+        dq2, dk2, dv2 = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ddq, ddk, ddv, ddsl = (torch.empty_like(dq), torch.empty_like(dkc),
+                               torch.empty_like(dvc), torch.empty_like(dsl))
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdq, hdk, hdv, hdsl))
+        d2h = ho.numel() * ho.element_size() + hdo.numel() * hdo.element_size()
+
+        def e2e_step():
+            dq2.copy_(hq, non_blocking=True)
+            dk2.copy_(hk, non_blocking=True)
+            dv2.copy_(hv, non_blocking=True)
+            oo = cga.prefill(dq2, dk2, dv2, causal=True)
+            ho.copy_(oo, non_blocking=True)
+            ddq.copy_(hdq, non_blocking=True)
+            ddk.copy_(hdk, non_blocking=True)
+            ddv.copy_(hdv, non_blocking=True)
+            ddsl.copy_(hdsl, non_blocking=True)
+            od = cga.decode(ddq, ddk, ddv, ddsl)
+            hdo.copy_(od, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e_steps = max(3, min(args.steps, 10))
+        barrier(world)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, world, dev)
+        e2e = {"value": pflops * world / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
+               "note": "prefill flops over the whole step incl. decode and host copies"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r = oracle_sample(args.cpu_seconds)
+        cpu = {"value": r["prefill_tflops"], "unit": "TFLOP/s", "cores": r["cores"],
+               "kind": "oracle", "sample": r["sample"], "decode_gbs": r["decode_gbs"]}
+
+    if rank == 0:
+        peak_t = pk["bf16_tflops"]
+        line = {
+            "metric": METRIC,
+            "value": tflops * world,
+            "unit": "TFLOP/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": step_ms,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic",
+            "config": config_block(),
+            "prefill": {"value": tflops, "unit": "TFLOP/s", "ms": pre_mean,
+                        "flops": pflops, "frac_of_bf16_peak": tflops / peak_t,
+                        "frac_of_bf16_sustained": tflops / pk["bf16_tflops_sustained"]},
+            "decode": {"value": dec_gbs, "unit": "GB/s", "ms": dec_mean, "bytes": dec_bytes,
+                       "roofline": {"bound": "hbm", "achieved": dec_gbs,
+                                    "peak": pk["hbm_gbs"], "unit": "GB/s",
+                                    "frac": dec_gbs / pk["hbm_gbs"], "traffic": None}},
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak_t,
+                         "unit": "TFLOP/s", "frac": tflops / peak_t, "traffic": None,
+                         "kernel": "prefill_tc_kernel", "peak_source": pk["source"]},
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+            "gpu_launches": 3 * args.steps,
+            "wall_s_timed_region": t_wall,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

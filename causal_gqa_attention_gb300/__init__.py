@@ -1,0 +1,199 @@
+"""Fused causal GQA attention forward for GB300 (sm_103a): prefill and split-KV decode.
+
+Two layers, both argument marshalling only (every step of the computation runs in the CUDA
+library built from ``csrc/``):
+
+* ``attn_prefill``, ``attn_prefill_ex``, ``attn_decode``, ``attn_decode_ex``, ... -- the C ABI of
+  ``include/gqa_attn.h`` under the same names, taking raw device pointers (ints) and sizes;
+  they return the C status code.
+* ``prefill(q, k, v, ...)`` and ``decode(q, kcache, vcache, seqlens, ...)`` -- the same calls on
+  torch CUDA tensors: shape/dtype checks, output allocation, the current torch stream; they
+  raise ``AttnError`` on a non-zero status.
+
+PyTorch provides device memory and streams only.
+"""
+from __future__ import annotations
+
+import math
+
+from . import _lib
+from ._lib import (ATTN_BF16, ATTN_DEV_SEQLEN_CLAMPED, ATTN_DEV_WAIT_TIMEOUT, ATTN_ERR_ALIGN,
+                   ATTN_ERR_CUDA, ATTN_ERR_INVALID, ATTN_ERR_TIMEOUT, ATTN_ERR_UNSUPPORTED,
+                   ATTN_ERR_WORKSPACE, ATTN_F32, ATTN_OK, AttnError)
+
+__all__ = [
+    "attn_prefill", "attn_prefill_ex", "attn_decode", "attn_decode_ex",
+    "attn_decode_workspace_bytes", "attn_decode_chunk_len", "attn_reserve_workspace",
+    "attn_device_status", "attn_status_string", "attn_version", "prefill", "decode",
+    "device_status", "AttnError", "ATTN_OK", "ATTN_ERR_INVALID", "ATTN_ERR_UNSUPPORTED",
+    "ATTN_ERR_ALIGN", "ATTN_ERR_WORKSPACE", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "ATTN_F32",
+    "ATTN_BF16", "ATTN_DEV_SEQLEN_CLAMPED", "ATTN_DEV_WAIT_TIMEOUT", "load_library",
+]
+
+
+def load_library():
+    return _lib.load()
+
+
+# ------------------------------------------------------------------ C ABI, same names
+
+
+def attn_prefill(q, k, v, o, lse, B, S, Hq, Hkv, D, scale, causal, stream):
+    return _lib.load().attn_prefill(q, k, v, o, lse, B, S, Hq, Hkv, D, scale, causal, stream)
+
+
+def attn_prefill_ex(q, k, v, o, lse, B, S, Hq, Hkv, D, scale, causal, in_dtype, out_dtype,
+                    stream):
+    return _lib.load().attn_prefill_ex(q, k, v, o, lse, B, S, Hq, Hkv, D, scale, causal,
+                                       in_dtype, out_dtype, stream)
+
+
+def attn_decode(q, kcache, vcache, seqlens, o, B, Hq, Hkv, D, max_len, scale, stream):
+    return _lib.load().attn_decode(q, kcache, vcache, seqlens, o, B, Hq, Hkv, D, max_len, scale,
+                                   stream)
+
+
+def attn_decode_ex(q, kcache, vcache, seqlens, o, lse, B, Hq, Hkv, D, max_len, scale, workspace,
+                   workspace_bytes, out_dtype, stream):
+    return _lib.load().attn_decode_ex(q, kcache, vcache, seqlens, o, lse, B, Hq, Hkv, D, max_len,
+                                      scale, workspace, workspace_bytes, out_dtype, stream)
+
+
+def attn_decode_workspace_bytes(B, Hq, Hkv, D, max_len):
+    return _lib.load().attn_decode_workspace_bytes(B, Hq, Hkv, D, max_len)
+
+
+def attn_decode_chunk_len(B, Hkv, max_len):
+    return _lib.load().attn_decode_chunk_len(B, Hkv, max_len)
+
+
+def attn_reserve_workspace(B, Hq, Hkv, D, max_len):
+    return _lib.load().attn_reserve_workspace(B, Hq, Hkv, D, max_len)
+
+
+def attn_device_status(stream, status_ptr):
+    return _lib.load().attn_device_status(stream, status_ptr)
+
+
+def attn_status_string(code):
+    return _lib.load().attn_status_string(code).decode()
+
+
+def attn_version():
+    return _lib.load().attn_version()
+
+
+# ------------------------------------------------------------------ torch tensor front end
+
+
+def _torch():
+    import torch
+
+    return torch
+
+
+def _stream_handle(device):
+    torch = _torch()
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _check_cuda(name, t, dtype=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def prefill(q, k, v, causal: bool = True, scale: float | None = None, out_dtype=None,
+            return_lse: bool = False, out=None, lse=None):
+    """Attention forward with q_len = kv_len.
+
+    q [B,Hq,S,D], k/v [B,Hkv,S,D], all bf16 (tensor-core path, D = 128) or all fp32 (fp32
+    CUDA-core path, D in {64,128}). ``out_dtype`` defaults to the input dtype (bf16 inputs may
+    ask for fp32 output: the result before the final rounding). Returns o, or (o, lse) with
+    lse [B,Hq,S] fp32 (natural log)."""
+    torch = _torch()
+    B, Hq, S, D = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (B, Hkv, S, D) or v.shape != k.shape:
+        raise ValueError(f"k/v shape {tuple(k.shape)}/{tuple(v.shape)} do not match q {tuple(q.shape)}")
+    if q.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("q/k/v must be bf16 or fp32")
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _check_cuda(n, t, q.dtype)
+    out_dtype = out_dtype or q.dtype
+    if out is None:
+        out = torch.empty((B, Hq, S, D), dtype=out_dtype, device=q.device)
+    else:
+        _check_cuda("out", out, out_dtype)
+    if return_lse and lse is None:
+        lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    in_t = ATTN_BF16 if q.dtype == torch.bfloat16 else ATTN_F32
+    out_t = ATTN_BF16 if out_dtype == torch.bfloat16 else ATTN_F32
+    with torch.cuda.device(q.device):
+        rc = attn_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, S, Hq, Hkv, D,
+                             float(scale), int(bool(causal)), in_t, out_t,
+                             _stream_handle(q.device))
+    _lib.check("attn_prefill_ex", rc)
+    return (out, lse) if return_lse else out
+
+
+def decode(q, kcache, vcache, seqlens, scale: float | None = None, out_dtype=None,
+           return_lse: bool = False, workspace=None, out=None, lse=None):
+    """One query token per sequence: q [B,Hq,D] bf16, caches [B,Hkv,max_len,D] bf16, seqlens
+    [B] int32 on the device. Returns o [B,Hq,D] (bf16 by default), or (o, lse [B,Hq]).
+
+    ``workspace``: optional uint8 CUDA tensor of at least ``attn_decode_workspace_bytes``;
+    without it the library-owned per-device buffer is used."""
+    torch = _torch()
+    B, Hq, D = q.shape
+    Hkv, max_len = kcache.shape[1], kcache.shape[2]
+    if kcache.shape != (B, Hkv, max_len, D) or vcache.shape != kcache.shape:
+        raise ValueError("cache shapes do not match q")
+    _check_cuda("q", q, torch.bfloat16)
+    _check_cuda("kcache", kcache, torch.bfloat16)
+    _check_cuda("vcache", vcache, torch.bfloat16)
+    _check_cuda("seqlens", seqlens, torch.int32)
+    if seqlens.shape != (B,):
+        raise ValueError("seqlens must be [B]")
+    out_dtype = out_dtype or torch.bfloat16
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=out_dtype, device=q.device)
+    else:
+        _check_cuda("out", out, out_dtype)
+    if return_lse and lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        _check_cuda("workspace", workspace)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    out_t = ATTN_BF16 if out_dtype == torch.bfloat16 else ATTN_F32
+    with torch.cuda.device(q.device):
+        rc = attn_decode_ex(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(seqlens), _ptr(out),
+                            _ptr(lse), B, Hq, Hkv, D, max_len, float(scale), ws_ptr, ws_bytes,
+                            out_t, _stream_handle(q.device))
+    _lib.check("attn_decode_ex", rc)
+    return (out, lse) if return_lse else out
+
+
+def device_status(device=None) -> int:
+    """Synchronise the current stream, then read and clear the device status word."""
+    import ctypes
+
+    torch = _torch()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    st = ctypes.c_uint(0)
+    with torch.cuda.device(dev):
+        rc = attn_device_status(_stream_handle(dev), ctypes.byref(st))
+    _lib.check("attn_device_status", rc)
+    return st.value

@@ -1,0 +1,289 @@
+// api.cu -- the C ABI declared in include/gqa_attn.h: host-side argument checks, tensor-map
+// encoding for the TMA loads, the library-owned decode workspace and the device status word.
+// Every check runs before the first CUDA call, so a rejected call touches no GPU state.
+#include "gqa_attn.h"
+#include "internal.h"
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+// Per-device status word written by the kernels (bits ATTN_DEV_*).
+__device__ unsigned int g_attn_status;
+
+namespace {
+
+using gqa::DecodeArgs;
+using gqa::PrefillTcArgs;
+
+constexpr int kMaxDevices = 64;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+bool scale_ok(float s) { return std::isfinite(s) && s > 0.f; }
+
+// ---- driver entry point for tensor-map encoding (no link-time dependency on libcuda)
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// bf16 tensor viewed as [planes, rows, 128] with a 64 x 128-row box, 128-byte swizzle.
+bool encode_bf16_rows(CUtensorMap *m, const void *base, long long planes, long long rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {128, (cuuint64_t)rows, (cuuint64_t)planes};
+    const cuuint64_t strides[2] = {128 * 2, (cuuint64_t)rows * 128 * 2};  // bytes, dims 1..2
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ---- device status word address, per device
+int status_ptr(unsigned **out)
+{
+    static unsigned *ptrs[kMaxDevices] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_attn_status) != cudaSuccess) return ATTN_ERR_CUDA;
+        ptrs[dev] = static_cast<unsigned *>(p);
+    }
+    *out = ptrs[dev];
+    return ATTN_OK;
+}
+
+// ---- library-owned decode workspace, per device
+struct Workspace {
+    void *ptr = nullptr;
+    size_t bytes = 0;
+};
+Workspace g_ws[kMaxDevices];
+std::mutex g_ws_mu;
+
+int workspace_acquire(size_t need, cudaStream_t stream, bool may_grow, void **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    Workspace &w = g_ws[dev];
+    if (w.bytes < need) {
+        if (!may_grow) return ATTN_ERR_WORKSPACE;
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return ATTN_ERR_CUDA;
+        if (cs != cudaStreamCaptureStatusNone) return ATTN_ERR_WORKSPACE;
+        if (w.ptr) {
+            if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
+            cudaFree(w.ptr);
+            w.ptr = nullptr;
+            w.bytes = 0;
+        }
+        size_t sz = need < (1u << 20) ? (1u << 20) : need;
+        if (cudaMalloc(&w.ptr, sz) != cudaSuccess) {
+            w.ptr = nullptr;
+            return ATTN_ERR_CUDA;
+        }
+        w.bytes = sz;
+    }
+    *out = w.ptr;
+    return ATTN_OK;
+}
+
+int check_prefill(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                  int S, int Hq, int Hkv, int D, float scale, int in_t, int out_t)
+{
+    if (!q || !k || !v || !o) return ATTN_ERR_INVALID;
+    if (B <= 0 || S <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID;
+    if (!scale_ok(scale)) return ATTN_ERR_INVALID;
+    if ((in_t != ATTN_F32 && in_t != ATTN_BF16) || (out_t != ATTN_F32 && out_t != ATTN_BF16))
+        return ATTN_ERR_INVALID;
+    if ((long long)B * Hq > (1LL << 30) || (long long)B * Hq * S > (1LL << 40))
+        return ATTN_ERR_UNSUPPORTED;
+    if (in_t == ATTN_BF16 && D != 128) return ATTN_ERR_UNSUPPORTED;
+    if (in_t == ATTN_BF16 && (long long)((S + 255) / 256) * B * Hq >= (1LL << 31))
+        return ATTN_ERR_UNSUPPORTED;
+    if (in_t == ATTN_F32 && ((D != 64 && D != 128) || out_t != ATTN_F32)) return ATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_ALIGN;
+    if (lse && !aligned4(lse)) return ATTN_ERR_ALIGN;
+    if (in_t == ATTN_F32 && (Hq > 65535 || B > 65535)) return ATTN_ERR_UNSUPPORTED;
+    return ATTN_OK;
+}
+
+int check_decode(const void *q, const void *kc, const void *vc, const int *seqlens, void *o,
+                 float *lse, int B, int Hq, int Hkv, int D, int max_len, float scale, int out_t)
+{
+    if (!q || !kc || !vc || !seqlens || !o) return ATTN_ERR_INVALID;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || max_len <= 0 || Hq % Hkv != 0)
+        return ATTN_ERR_INVALID;
+    if (!scale_ok(scale)) return ATTN_ERR_INVALID;
+    if (out_t != ATTN_F32 && out_t != ATTN_BF16) return ATTN_ERR_INVALID;
+    if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+    if (B > 65535 || (long long)Hkv * (Hq / Hkv) > 65535) return ATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(kc) || !aligned16(vc) || !aligned16(o)) return ATTN_ERR_ALIGN;
+    if (!aligned4(seqlens) || (lse && !aligned4(lse))) return ATTN_ERR_ALIGN;
+    return ATTN_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int attn_version(void) { return 100; }
+
+const char *attn_status_string(int s)
+{
+    switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case ATTN_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case ATTN_ERR_WORKSPACE: return "decode workspace too small";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+    }
+}
+
+int attn_prefill_ex(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                    int S, int Hq, int Hkv, int D, float scale, int causal, int in_dtype,
+                    int out_dtype, void *stream)
+{
+    int rc = check_prefill(q, k, v, o, lse, B, S, Hq, Hkv, D, scale, in_dtype, out_dtype);
+    if (rc != ATTN_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (in_dtype == ATTN_F32)
+        return cuda_status(gqa::launch_prefill_f32(
+            static_cast<const float *>(q), static_cast<const float *>(k),
+            static_cast<const float *>(v), static_cast<float *>(o), lse, B, S, Hq, Hkv, D, scale,
+            causal ? 1 : 0, st));
+    PrefillTcArgs a;
+    std::memset(&a, 0, sizeof(a));
+    if (!encode_bf16_rows(&a.tq, q, (long long)B * Hq, S) ||
+        !encode_bf16_rows(&a.tk, k, (long long)B * Hkv, S) ||
+        !encode_bf16_rows(&a.tv, v, (long long)B * Hkv, S))
+        return ATTN_ERR_CUDA;
+    a.o = o;
+    a.lse = lse;
+    a.B = B;
+    a.S = S;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.causal = causal ? 1 : 0;
+    rc = status_ptr(&a.status);
+    if (rc != ATTN_OK) return rc;
+    return cuda_status(gqa::launch_prefill_tc(a, out_dtype == ATTN_F32, st));
+}
+
+int attn_prefill(const void *q, const void *k, const void *v, void *o, float *lse, int B, int S,
+                 int Hq, int Hkv, int D, float scale, int causal, void *stream)
+{
+    return attn_prefill_ex(q, k, v, o, lse, B, S, Hq, Hkv, D, scale, causal, ATTN_BF16, ATTN_BF16,
+                           stream);
+}
+
+int attn_decode_chunk_len(int B, int Hkv, int max_len)
+{
+    if (B <= 0 || Hkv <= 0 || max_len <= 0) return 0;
+    return gqa::decode_chunk_len(B, Hkv, max_len);
+}
+
+size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int max_len)
+{
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || max_len <= 0 || Hq % Hkv != 0) return 0;
+    return gqa::decode_workspace_bytes(B, Hq, D, max_len, gqa::decode_chunk_len(B, Hkv, max_len));
+}
+
+int attn_reserve_workspace(int B, int Hq, int Hkv, int D, int max_len)
+{
+    const size_t need = attn_decode_workspace_bytes(B, Hq, Hkv, D, max_len);
+    if (need == 0) return ATTN_ERR_INVALID;
+    void *p = nullptr;
+    return workspace_acquire(need, nullptr, true, &p);
+}
+
+int attn_decode_ex(const void *q, const void *kcache, const void *vcache, const int *seqlens,
+                   void *o, float *lse, int B, int Hq, int Hkv, int D, int max_len, float scale,
+                   void *workspace, size_t workspace_bytes, int out_dtype, void *stream)
+{
+    int rc = check_decode(q, kcache, vcache, seqlens, o, lse, B, Hq, Hkv, D, max_len, scale,
+                          out_dtype);
+    if (rc != ATTN_OK) return rc;
+    const int chunk = gqa::decode_chunk_len(B, Hkv, max_len);
+    const size_t need = gqa::decode_workspace_bytes(B, Hq, D, max_len, chunk);
+    if (workspace != nullptr) {
+        if (workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    void *ws = workspace;
+    if (ws == nullptr) {
+        rc = workspace_acquire(need, st, true, &ws);
+        if (rc != ATTN_OK) return rc;
+    }
+    DecodeArgs a;
+    a.q = q;
+    a.kc = kcache;
+    a.vc = vcache;
+    a.seqlens = seqlens;
+    a.o = o;
+    a.lse = lse;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.max_len = max_len;
+    a.chunk = chunk;
+    a.nsplit = (max_len + chunk - 1) / chunk;
+    a.ws_o = static_cast<float *>(ws);
+    a.ws_ml = reinterpret_cast<float2 *>(static_cast<char *>(ws) +
+                                         (size_t)B * Hq * a.nsplit * D * sizeof(float));
+    a.scale_log2 = scale * 1.4426950408889634f;
+    rc = status_ptr(&a.status);
+    if (rc != ATTN_OK) return rc;
+    return cuda_status(gqa::launch_decode(a, out_dtype == ATTN_F32, st));
+}
+
+int attn_decode(const void *q, const void *kcache, const void *vcache, const int *seqlens,
+                void *o, int B, int Hq, int Hkv, int D, int max_len, float scale, void *stream)
+{
+    return attn_decode_ex(q, kcache, vcache, seqlens, o, nullptr, B, Hq, Hkv, D, max_len, scale,
+                          nullptr, 0, ATTN_BF16, stream);
+}
+
+int attn_device_status(void *stream, unsigned int *status)
+{
+    if (!status) return ATTN_ERR_INVALID;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_attn_status, sizeof(v)) != cudaSuccess) return ATTN_ERR_CUDA;
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_attn_status, &zero, sizeof(zero)) != cudaSuccess) return ATTN_ERR_CUDA;
+    *status = v;
+    return ATTN_OK;
+}
+
+}  // extern "C"

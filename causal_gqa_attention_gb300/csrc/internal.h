@@ -1,0 +1,51 @@
+// internal.h -- launchers shared between the C-ABI layer (api.cu) and the kernel files.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace gqa {
+
+// Prefill on tcgen05 tensor cores: bf16 q/k/v with head dim 128. The tensor maps describe
+// q [B*Hq, S, 128], k and v [B*Hkv, S, 128] as 3-D bf16 tensors with 64x128 boxes and
+// 128-byte swizzle.
+struct PrefillTcArgs {
+    CUtensorMap tq, tk, tv;
+    void *o;        // [B, Hq, S, 128], bf16 or fp32
+    float *lse;     // [B, Hq, S] or nullptr
+    int B, S, Hq, Hkv;
+    float scale_log2;  // scale * log2(e)
+    int causal;
+    unsigned *status;  // device status word
+};
+cudaError_t launch_prefill_tc(const PrefillTcArgs &a, bool out_f32, cudaStream_t stream);
+int prefill_tc_smem_bytes();
+
+// Prefill on CUDA cores in fp32 (fp32 q/k/v/o), head dim 64 or 128.
+cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, float *o,
+                               float *lse, int B, int S, int Hq, int Hkv, int D, float scale,
+                               int causal, cudaStream_t stream);
+
+// Decode: split kernel over (chunk, kv head [, query-head subgroup], batch) writing partial
+// (m, l, o) per chunk into the workspace, then the merge kernel.
+struct DecodeArgs {
+    const void *q;        // [B, Hq, D] bf16
+    const void *kc, *vc;  // [B, Hkv, max_len, D] bf16
+    const int *seqlens;   // [B]
+    void *o;              // [B, Hq, D] bf16 or fp32
+    float *lse;           // [B, Hq] or nullptr
+    float *ws_o;          // [B, Hq, nsplit, D]
+    float2 *ws_ml;        // [B, Hq, nsplit]: (max in log2 units, sum)
+    int B, Hq, Hkv, D, max_len, chunk, nsplit;
+    float scale_log2;
+    unsigned *status;
+};
+cudaError_t launch_decode(const DecodeArgs &a, bool out_f32, cudaStream_t stream);
+
+// Decode work split, shared by the workspace query and the launch.
+int decode_chunk_len(int B, int Hkv, int max_len);
+size_t decode_workspace_bytes(int B, int Hq, int D, int max_len, int chunk);
+
+}  // namespace gqa

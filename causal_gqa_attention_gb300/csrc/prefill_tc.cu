@@ -1,0 +1,371 @@
+// prefill_tc.cu -- fused attention forward (prefill) on sm_103a tensor cores, bf16 in,
+// fp32 accumulation and softmax state, head dim 128.
+//
+// One thread block owns 256 consecutive query rows of one (batch, query head): two 128-row
+// Q tiles. Both tiles consume the same stream of 128-key K/V tiles, so every K/V tile brought
+// in by TMA feeds four 128x128x128 tensor-core products. Roles (12 warps):
+//   warp 0      TMA producer: Q tiles once, then K_j and V_j into a 2-stage ring each;
+//   warp 1      tcgen05 issuer (one thread): S_t = Q_t K_j^T into TMEM, O_t += P_t V_j with
+//               P_t read from TMEM; owns the TMEM allocation;
+//   warps 4-7   softmax for tile 0, warps 8-11 for tile 1: one thread per query row (its TMEM
+//               lane). Reads the 128 scores of its row, masks, updates the running max and
+//               sum, writes P (bf16) over the scores it came from, rescales its O row when
+//               the max moved, and finally writes O / l and the LSE.
+// TMEM (512 columns): S_0 | S_1 | O_0 | O_1, 128 fp32 columns each; P_t is packed bf16 in the
+// first 64 columns of S_t. S and P never leave the SM.
+//
+// The two tiles alternate on the tensor core: while tile 0's softmax runs, the tensor core
+// computes tile 1's P V and next S, and the other way round. Issue order per key tile j:
+//   [PV_0(j-1)] S_0(j) [PV_1(j-1)] S_1(j)
+// tcgen05 operations of one thread complete in issue order, so the commit that signals
+// "S_t(j) ready" also guarantees PV_t(j-1) finished: the softmax may then overwrite P_t and
+// rescale O_t without a separate barrier.
+//
+// Rescaling is lazy: a row keeps its reference max until the true max exceeds it by more than
+// 2^8 (scores are in log2 units), so the O row in TMEM is rescaled only then. The result is
+// the same in exact arithmetic because the same reference is used for O and l.
+//
+// Sources: "Attention three-op fusion" (xdnf.cn/news/349386): section 1.1 and 1.2 (S = QK^T
+// scale, softmax, O = PV; S and P must stay on chip), section 2.2-2.3 (running max and sum,
+// correction factor exp(m - m_new) applied to the accumulated output, one division by l at the
+// end), section 3.3 and 5.5 (m, l and the accumulator in fp32), section 4.3 (causal mask: key
+// tiles above the diagonal are skipped, the diagonal tile is masked per element with -inf),
+// section 6.1 (ragged tail: out-of-range K/V rows read as 0, their scores set to -inf);
+// "triton-optimization" skill (skillsmp.com) section 3.5 (LSE = m + log l).
+#include "internal.h"
+#include "ptx.cuh"
+
+#include <cmath>
+
+namespace gqa {
+namespace {
+
+constexpr int BM = 128;        // query rows per tile = TMEM lanes
+constexpr int BN = 128;        // keys per K/V tile
+constexpr int HD = 128;        // head dim
+constexpr int kThreads = 384;  // 12 warps
+constexpr uint32_t kBox = 16384;          // one 128-row x 64-col bf16 box (128-byte rows)
+constexpr uint32_t kTile = 2 * kBox;      // 128 x 128 bf16
+constexpr uint32_t kOffQ = 0;             // 2 tiles
+constexpr uint32_t kOffK = 2 * kTile;     // 2 stages
+constexpr uint32_t kOffV = 4 * kTile;     // 2 stages
+constexpr uint32_t kOffBar = 6 * kTile;
+constexpr uint32_t kSmem = kOffBar + 256 + 1024;  // + barriers, + alignment slack
+constexpr float kRescaleThreshold = 8.0f;         // log2 units
+
+// TMEM column bases
+constexpr uint32_t kColS = 0;    // + 128 t
+constexpr uint32_t kColO = 256;  // + 128 t
+
+// barrier indices
+enum : int {
+    B_Q = 0,
+    B_KFULL = 1,   // 2
+    B_KEMPTY = 3,  // 2
+    B_VFULL = 5,   // 2
+    B_VEMPTY = 7,  // 2
+    B_SFULL = 9,   // 2 (per tile)
+    B_PFULL = 11,  // 2 (per tile)
+    B_OFULL = 13,  // 2 (per tile)
+    B_DRAIN = 15,
+    NUM_BARS = 16
+};
+
+__device__ __forceinline__ int last_key_tile(int causal, int q_first, int nkv)
+{
+    // causal: the tile whose rows start at q_first needs keys up to q_first + 127
+    return causal ? min((q_first + BM - 1) / BN, nkv - 1) : nkv - 1;
+}
+
+template <bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                      const __grid_constant__ CUtensorMap tv, void *__restrict__ out,
+                      float *__restrict__ lse, int B, int S, int Hq, int Hkv, float scale_log2,
+                      int causal, unsigned *__restrict__ status)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + NUM_BARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+    // ---- work item: heaviest row blocks first (causal), heads of one group adjacent
+    const int n_rb = (S + 2 * BM - 1) / (2 * BM);
+    const int idx = blockIdx.x;
+    const int rb = n_rb - 1 - idx / (Hq * B);
+    const int hb = idx % (Hq * B);
+    const int h = hb % Hq, b = hb / Hq;
+    const int g = h / (Hq / Hkv);
+    const int q0 = rb * 2 * BM;
+    const int nkv = (S + BN - 1) / BN;
+    const int n_tiles = (q0 + BM < S) ? 2 : 1;
+    int last_j[2];
+    last_j[0] = last_key_tile(causal, q0, nkv);
+    last_j[1] = (n_tiles == 2) ? last_key_tile(causal, q0 + BM, nkv) : -1;
+    const int n_j = max(last_j[0], last_j[1]) + 1;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bar[B_Q], 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bar[B_KFULL + s], 1);
+            mbar_init(&bar[B_KEMPTY + s], 1);
+            mbar_init(&bar[B_VFULL + s], 1);
+            mbar_init(&bar[B_VEMPTY + s], 1);
+            mbar_init(&bar[B_SFULL + s], 1);
+            mbar_init(&bar[B_PFULL + s], BM);
+            mbar_init(&bar[B_OFULL + s], 1);
+        }
+        mbar_init(&bar[B_DRAIN], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ================================================================ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tq);
+            tma_prefetch_desc(&tk);
+            tma_prefetch_desc(&tv);
+            const int zq = b * Hq + h, zk = b * Hkv + g;
+            mbar_arrive_expect_tx(&bar[B_Q], n_tiles * kTile);
+            for (int t = 0; t < n_tiles; ++t)
+                for (int x = 0; x < 2; ++x)
+                    tma_load_3d(smem + kOffQ + t * kTile + x * kBox, &tq, &bar[B_Q], x * 64,
+                                q0 + t * BM, zq);
+            int issued_k[2] = {0, 0}, issued_v[2] = {0, 0};
+            for (int j = 0; j < n_j; ++j) {
+                const int s = j & 1, use = j >> 1;
+                if (use > 0 && !mbar_wait(&bar[B_KEMPTY + s], (use - 1) & 1, abort_flag)) break;
+                mbar_arrive_expect_tx(&bar[B_KFULL + s], kTile);
+                for (int x = 0; x < 2; ++x)
+                    tma_load_3d(smem + kOffK + s * kTile + x * kBox, &tk, &bar[B_KFULL + s],
+                                x * 64, j * BN, zk);
+                issued_k[s] = use + 1;
+                if (use > 0 && !mbar_wait(&bar[B_VEMPTY + s], (use - 1) & 1, abort_flag)) break;
+                mbar_arrive_expect_tx(&bar[B_VFULL + s], kTile);
+                for (int x = 0; x < 2; ++x)
+                    tma_load_3d(smem + kOffV + s * kTile + x * kBox, &tv, &bar[B_VFULL + s],
+                                x * 64, j * BN, zk);
+                issued_v[s] = use + 1;
+            }
+            if (*abort_flag) {
+                // let every copy this block started land before the block exits
+                volatile int never = 0;
+                mbar_wait(&bar[B_Q], 0, &never);
+                for (int s = 0; s < 2; ++s) {
+                    if (issued_k[s]) mbar_wait(&bar[B_KFULL + s], (issued_k[s] - 1) & 1, &never);
+                    if (issued_v[s]) mbar_wait(&bar[B_VFULL + s], (issued_v[s] - 1) & 1, &never);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ================================================================ tcgen05 issuer
+        if (lane == 0) {
+            constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0, 0);  // Q, K both K-major
+            constexpr uint32_t idO = idesc_bf16_f32(BM, HD, 0, 1);  // P from TMEM, V MN-major
+            const uint32_t sQ = smem_u32(smem + kOffQ);
+            const uint32_t sK = smem_u32(smem + kOffK);
+            const uint32_t sV = smem_u32(smem + kOffV);
+            bool ok = mbar_wait(&bar[B_Q], 0, abort_flag);
+            for (int j = 0; ok && j <= n_j; ++j) {
+                const bool do_s = j < n_j;
+                const bool do_pv = j >= 1;
+                if (do_s && !mbar_wait(&bar[B_KFULL + (j & 1)], (j >> 1) & 1, abort_flag)) break;
+                if (do_pv &&
+                    !mbar_wait(&bar[B_VFULL + ((j - 1) & 1)], ((j - 1) >> 1) & 1, abort_flag))
+                    break;
+                tc_fence_after();
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (do_pv && j - 1 <= last_j[t]) {
+                        if (!mbar_wait(&bar[B_PFULL + t], (j - 1) & 1, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t vbase = sV + ((j - 1) & 1) * kTile;
+#pragma unroll
+                        for (int kk = 0; kk < BN / 16; ++kk) {
+                            // B = V rows 16kk..16kk+15: MN-major, 64-col chunks 16 KB apart,
+                            // 8-row groups 1 KB apart
+                            const uint64_t bd = smem_desc_sw128(vbase + kk * 2048, kBox, 1024);
+                            mma_ts(tmem + kColO + t * 128, tmem + kColS + t * 128 + kk * 8, bd,
+                                   idO, (j - 1 > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        if (j - 1 == last_j[t]) mma_commit(&bar[B_OFULL + t]);
+                    }
+                    if (do_s && j <= last_j[t]) {
+                        const uint32_t qbase = sQ + t * kTile;
+                        const uint32_t kbase = sK + (j & 1) * kTile;
+#pragma unroll
+                        for (int kk = 0; kk < HD / 16; ++kk) {
+                            const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+                            const uint64_t ad = smem_desc_sw128(qbase + off, 16, 1024);
+                            const uint64_t bd = smem_desc_sw128(kbase + off, 16, 1024);
+                            mma_ss(tmem + kColS + t * 128, ad, bd, idS, kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit(&bar[B_SFULL + t]);
+                    }
+                }
+                if (!ok) break;
+                if (do_s) mma_commit(&bar[B_KEMPTY + (j & 1)]);
+                if (do_pv) mma_commit(&bar[B_VEMPTY + ((j - 1) & 1)]);
+            }
+            // drain: all issued tcgen05 work finishes before TMEM is released
+            mma_commit(&bar[B_DRAIN]);
+            volatile int never = 0;
+            mbar_wait(&bar[B_DRAIN], 0, &never);
+        }
+    } else if (warp >= 4) {
+        // ================================================================ softmax / epilogue
+        const int t = (warp - 4) / 4;
+        const int wq = warp & 3;
+        const int r = wq * 32 + lane;  // row within the tile = TMEM lane
+        const int i = q0 + t * BM + r;  // query row
+        const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
+        const uint32_t tS = lane_base + kColS + t * 128;
+        const uint32_t tO = lane_base + kColO + t * 128;
+        if (t < n_tiles) {
+            float m_ref = -INFINITY, l = 0.f;
+            bool ok = true;
+            for (int j = 0; j <= last_j[t]; ++j) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_SFULL + t], j & 1, abort_flag));
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t sv[128];  // raw fp32 bits of the row's scores
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, &sv[c * 32]);
+                const int k0 = j * BN;
+                if (k0 + BN > S || (causal && k0 + BN - 1 > i)) {
+                    const int lim = causal ? min(i + 1, S) : S;  // keys < lim are visible
+#pragma unroll
+                    for (int c = 0; c < 128; ++c)
+                        if (k0 + c >= lim) sv[c] = __float_as_uint(-INFINITY);
+                }
+                float mx = __uint_as_float(sv[0]);
+#pragma unroll
+                for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sv[c]));
+                const float m_cand = mx * scale_log2;
+                const bool need = m_cand > m_ref + kRescaleThreshold;
+                const float m_new = need ? m_cand : m_ref;
+                const float mu = (m_new == -INFINITY) ? 0.f : m_new;
+                const float alpha = ex2(m_ref - mu);
+                float rs = 0.f;
+                uint32_t pk[64];
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    const float p0 = ex2(fmaf(__uint_as_float(sv[2 * c]), scale_log2, -mu));
+                    const float p1 = ex2(fmaf(__uint_as_float(sv[2 * c + 1]), scale_log2, -mu));
+                    rs += p0 + p1;
+                    pk[c] = pack_bf16x2(p0, p1);
+                }
+                l = fmaf(l, alpha, rs);
+                tmem_st32(tS, &pk[0]);
+                tmem_st32(tS + 32, &pk[32]);
+                if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t ov[32];
+                        tmem_ld32(tO + c * 32, ov);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                        tmem_st32(tO + c * 32, ov);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&bar[B_PFULL + t]);
+                m_ref = m_new;
+            }
+            if (ok)
+                ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_OFULL + t], 0, abort_flag));
+            if (ok) {
+                tc_fence_after();
+                const bool live = i < S;
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const size_t orow = ((size_t)b * Hq + h) * S + (live ? i : 0);
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t ov[32];
+                    tmem_ld32(tO + c * 32, ov);
+                    if (!live) continue;
+                    if (OUT_F32) {
+                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(out) +
+                                                                 orow * HD + c * 32);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            dst[e] = make_float4(__uint_as_float(ov[4 * e]) * inv,
+                                                 __uint_as_float(ov[4 * e + 1]) * inv,
+                                                 __uint_as_float(ov[4 * e + 2]) * inv,
+                                                 __uint_as_float(ov[4 * e + 3]) * inv);
+                    } else {
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(out) +
+                                                               orow * HD + c * 32);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int f = 0; f < 4; ++f)
+                                w[f] = pack_bf16x2(__uint_as_float(ov[8 * e + 2 * f]) * inv,
+                                                   __uint_as_float(ov[8 * e + 2 * f + 1]) * inv);
+                            dst[e] = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    }
+                }
+                if (live && lse != nullptr)
+                    lse[orow] = l > 0.f ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+    if (threadIdx.x == 0 && *abort_flag) atomicOr(status, 2u);
+}
+
+template <bool OUT_F32>
+cudaError_t launch_t(const PrefillTcArgs &a, cudaStream_t st)
+{
+    static bool attr_set[64] = {};  // the attribute is set once per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 64 || !attr_set[dev]) {
+        e = cudaFuncSetAttribute(prefill_tc_kernel<OUT_F32>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        if (e != cudaSuccess) return e;
+        if (dev < 64) attr_set[dev] = true;
+    }
+    const int n_rb = (a.S + 2 * BM - 1) / (2 * BM);
+    const long long blocks = (long long)n_rb * a.Hq * a.B;
+    prefill_tc_kernel<OUT_F32><<<(unsigned)blocks, kThreads, kSmem, st>>>(
+        a.tq, a.tk, a.tv, a.o, a.lse, a.B, a.S, a.Hq, a.Hkv, a.scale_log2, a.causal, a.status);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int prefill_tc_smem_bytes() { return (int)kSmem; }
+
+cudaError_t launch_prefill_tc(const PrefillTcArgs &a, bool out_f32, cudaStream_t st)
+{
+    return out_f32 ? launch_t<true>(a, st) : launch_t<false>(a, st);
+}
+
+}  // namespace gqa

@@ -1,0 +1,144 @@
+/*
+ * gqa_attn.h -- C ABI of the fused attention-forward library for GB300 (sm_103a).
+ *
+ * Two regimes share one library:
+ *   prefill: q_len = kv_len = S, optional causal mask, O = softmax(Q K^T * scale) V per head,
+ *            computed as one fused kernel that never writes the score or probability matrix
+ *            to device memory;
+ *   decode:  one query token per sequence against a KV cache; the keys are split into chunks
+ *            processed by separate thread blocks, and a second kernel merges the chunk results
+ *            with their log-sum-exp weights.
+ *
+ * The operation (per batch b, query head h, query row i):
+ *   g = h / (Hq / Hkv)                                      kv head of h (contiguous groups)
+ *   s_j = scale * sum_d q[b,h,i,d] k[b,g,j,d]               scores
+ *   visible keys: j < kv_len, and j <= i when causal        masked scores are -infinity
+ *   O[b,h,i,:] = sum_j softmax(s)_j v[b,g,j,:]              row softmax, then P V
+ *   LSE[b,h,i] = log sum_j exp(s_j)                         natural log, of the scaled scores
+ * Sources: "Attention three-op fusion" (xdnf.cn/news/349386) section 1.1 (the S, P, O chain),
+ * section 2.2-2.3 (online softmax with running max and sum, output correction, divide once at
+ * the end), section 4.3 (causal and padding masks as -infinity) and section 4.4 (keys split
+ * across thread blocks, partial results merged); "Hand-written Triton decoder"
+ * (m.nlpx.cn/news/28229) section 2.1 (2 KV heads broadcast to 8 query heads, head dim 128)
+ * and section 3.3 (partials in a separate buffer reduced by a second small kernel);
+ * "triton-optimization" skill (skillsmp.com) section 3.5 (log-sum-exp = m + log of the sum).
+ *
+ * Conventions for every entry point:
+ *   - All tensors are device pointers, row-major with the head dimension D innermost and
+ *     contiguous; the caller owns them. The library never frees caller memory.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Calls are asynchronous on
+ *     that stream; nothing is allocated and nothing synchronizes on the hot path, except the
+ *     documented first-use growth of the library-owned decode workspace.
+ *   - Arguments are checked on the host before anything is launched. A bad argument returns
+ *     an error code and launches nothing. A launch failure returns ATTN_ERR_CUDA.
+ *   - Conditions only the device can see (a sequence length above max_len, a pipeline wait
+ *     that ran out) set bits of a per-device status word; read it with attn_device_status.
+ *   - Results are deterministic for fixed inputs and shapes (no floating-point atomics).
+ */
+#ifndef GQA_ATTN_H
+#define GQA_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID = 1,     /* NULL pointer, non-positive size, Hq % Hkv != 0, bad dtype   */
+    ATTN_ERR_UNSUPPORTED = 2, /* valid but not built: head dim or dtype combination          */
+    ATTN_ERR_ALIGN = 3,       /* a tensor pointer is not 16-byte aligned                     */
+    ATTN_ERR_WORKSPACE = 4,   /* decode workspace too small (or cannot grow while capturing) */
+    ATTN_ERR_CUDA = 5,        /* a CUDA runtime or driver call failed                        */
+    ATTN_ERR_TIMEOUT = 6      /* reported through attn_device_status: a device wait expired  */
+} attn_status;
+
+/* Element types. */
+typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype;
+
+/* Bits of the device status word (attn_device_status). */
+#define ATTN_DEV_SEQLEN_CLAMPED 0x1u /* decode: a seqlens[b] was < 0 or > max_len; clamped   */
+#define ATTN_DEV_WAIT_TIMEOUT 0x2u   /* prefill: a pipeline wait ran out; the block stopped  */
+
+/*
+ * attn_prefill -- causal or non-causal prefill, bf16 in, bf16 out.
+ *   q   [B, Hq,  S, D] bf16        k, v [B, Hkv, S, D] bf16
+ *   o   [B, Hq,  S, D] bf16        lse  [B, Hq, S] fp32, natural log; may be NULL
+ *   scale multiplies the scores before the softmax (usually 1/sqrt(D)).
+ *   causal != 0: query i sees keys 0..i.
+ * Requires Hq % Hkv == 0, D == 128, 16-byte aligned pointers.
+ * Computes on tcgen05 tensor cores (bf16 products, fp32 accumulation and softmax state);
+ * the probabilities are rounded to bf16 before the P V product.
+ */
+int attn_prefill(const void *q, const void *k, const void *v, void *o, float *lse, int B, int S,
+                 int Hq, int Hkv, int D, float scale, int causal, void *stream);
+
+/*
+ * attn_prefill_ex -- prefill with explicit element types.
+ *   in_dtype  ATTN_BF16: q, k, v bf16; D == 128; tensor-core kernel (as attn_prefill).
+ *             ATTN_F32:  q, k, v fp32; D in {64, 128}; fp32 CUDA-core kernel (fp32 products,
+ *                        sums and exponentials throughout).
+ *   out_dtype ATTN_BF16 or ATTN_F32 for o (ATTN_F32 with bf16 inputs returns the fp32 result
+ *             before the final rounding). fp32 inputs require out_dtype ATTN_F32.
+ * Other arguments as attn_prefill.
+ */
+int attn_prefill_ex(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                    int S, int Hq, int Hkv, int D, float scale, int causal, int in_dtype,
+                    int out_dtype, void *stream);
+
+/*
+ * attn_decode -- one query token per sequence against a bf16 KV cache.
+ *   q        [B, Hq, D] bf16
+ *   kcache   [B, Hkv, max_len, D] bf16, vcache likewise; rows >= seqlens[b] are never read
+ *   seqlens  [B] int32, device memory: valid cache rows of sequence b (including the newest
+ *            token, already written); 0 gives o = 0 (and lse = -inf)
+ *   o        [B, Hq, D] bf16
+ * Requires Hq % Hkv == 0, D in {64, 128}, max_len >= 1.
+ * Scratch for the per-chunk partial results comes from a library-owned buffer per device.
+ * The first call for a larger shape grows it (cudaMalloc, with a device synchronisation);
+ * during stream capture it cannot grow and the call returns ATTN_ERR_WORKSPACE instead, so
+ * reserve it first with attn_reserve_workspace. Calls on different streams of one device
+ * share that buffer: serialise them, or use attn_decode_ex with your own workspace.
+ */
+int attn_decode(const void *q, const void *kcache, const void *vcache, const int *seqlens,
+                void *o, int B, int Hq, int Hkv, int D, int max_len, float scale, void *stream);
+
+/*
+ * attn_decode_ex -- decode with an optional fp32 LSE output [B, Hq] (lse may be NULL), a
+ * caller-owned device workspace of at least attn_decode_workspace_bytes(...) bytes (16-byte
+ * aligned; NULL = the library-owned buffer, as attn_decode), and out_dtype ATTN_BF16 or
+ * ATTN_F32 for o. A workspace that is too small returns ATTN_ERR_WORKSPACE.
+ */
+int attn_decode_ex(const void *q, const void *kcache, const void *vcache, const int *seqlens,
+                   void *o, float *lse, int B, int Hq, int Hkv, int D, int max_len, float scale,
+                   void *workspace, size_t workspace_bytes, int out_dtype, void *stream);
+
+/* Workspace bytes attn_decode_ex needs for this shape (0 for invalid arguments).
+ * Depends only on the arguments, not on the device. */
+size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int max_len);
+
+/* Keys per chunk (one thread block each) that decode uses for this shape (0 if invalid). */
+int attn_decode_chunk_len(int B, int Hkv, int max_len);
+
+/* Grow the library-owned decode workspace of the current device to fit this shape. Call it
+ * before capturing attn_decode in a CUDA graph. Synchronises the device when it grows. */
+int attn_reserve_workspace(int B, int Hq, int Hkv, int D, int max_len);
+
+/* Synchronise `stream`, then read and clear the current device's status word into *status
+ * (bits ATTN_DEV_*). Returns ATTN_OK, or ATTN_ERR_CUDA if the synchronisation failed. */
+int attn_device_status(void *stream, unsigned int *status);
+
+/* Static text for a return code. */
+const char *attn_status_string(int status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_ATTN_H */

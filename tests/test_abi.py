@@ -1,0 +1,103 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol the header declares,
+and rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "gqa_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from causal_gqa_attention_gb300 import _lib, build
+
+    build.build()
+    return _lib.load()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_ ]*[\s\*]+([a-z_][a-z0-9_]*)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(n for n in names if n.startswith("attn_")))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ("attn_prefill", "attn_decode", "attn_prefill_ex", "attn_decode_ex"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from causal_gqa_attention_gb300 import _lib
+
+    names = _declared_functions()
+    for n in names:
+        assert hasattr(lib, n), f"missing export {n}"
+    assert set(names) == set(_lib.SIGNATURES), "binding and header disagree"
+    import causal_gqa_attention_gb300 as cga
+
+    for n in names:
+        assert callable(getattr(cga, n)), f"binding lacks {n}"
+
+
+def test_status_strings_and_version(lib):
+    assert lib.attn_version() >= 100
+    assert lib.attn_status_string(0) == b"ok"
+    for code in range(1, 7):
+        assert lib.attn_status_string(code) not in (b"ok", b"unknown status")
+
+
+A16 = 1 << 20  # a 16-byte aligned fake device address; never dereferenced (rejected before)
+
+
+@pytest.mark.parametrize("args,code", [
+    # q, k, v, o, lse, B, S, Hq, Hkv, D, scale, causal, in, out
+    ((0, A16, A16, A16, None, 1, 8, 2, 1, 128, 0.1, 1, 1, 1), 1),   # NULL q
+    ((A16, A16, A16, A16, None, 0, 8, 2, 1, 128, 0.1, 1, 1, 1), 1),  # B = 0
+    ((A16, A16, A16, A16, None, 1, 0, 2, 1, 128, 0.1, 1, 1, 1), 1),  # S = 0
+    ((A16, A16, A16, A16, None, 1, 8, 3, 2, 128, 0.1, 1, 1, 1), 1),  # Hq % Hkv
+    ((A16, A16, A16, A16, None, 1, 8, 2, 1, 128, 0.0, 1, 1, 1), 1),  # scale 0
+    ((A16, A16, A16, A16, None, 1, 8, 2, 1, 128, float("nan"), 1, 1, 1), 1),
+    ((A16, A16, A16, A16, None, 1, 8, 2, 1, 128, 0.1, 1, 7, 1), 1),  # bad dtype
+    ((A16, A16, A16, A16, None, 1, 8, 2, 1, 64, 0.1, 1, 1, 1), 2),   # bf16 needs D = 128
+    ((A16, A16, A16, A16, None, 1, 8, 2, 1, 96, 0.1, 1, 0, 0), 2),   # fp32 D = 96
+    ((A16, A16, A16, A16, None, 1, 8, 2, 1, 64, 0.1, 1, 0, 1), 2),   # fp32 in, bf16 out
+    ((A16 + 8, A16, A16, A16, None, 1, 8, 2, 1, 128, 0.1, 1, 1, 1), 3),  # misaligned q
+    ((A16, A16, A16, A16, A16 + 2, 1, 8, 2, 1, 128, 0.1, 1, 1, 1), 3),  # misaligned lse
+])
+def test_prefill_rejects_on_host(lib, args, code):
+    assert lib.attn_prefill_ex(*args, None) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    # q, kc, vc, seqlens, o, lse, B, Hq, Hkv, D, max_len, scale, ws, ws_bytes, out
+    ((A16, A16, A16, None, A16, None, 2, 8, 2, 128, 64, 0.1, None, 0, 1), 1),  # NULL seqlens
+    ((A16, A16, A16, A16, A16, None, 2, 8, 3, 128, 64, 0.1, None, 0, 1), 1),   # Hq % Hkv
+    ((A16, A16, A16, A16, A16, None, 2, 8, 2, 128, 0, 0.1, None, 0, 1), 1),    # max_len 0
+    ((A16, A16, A16, A16, A16, None, 2, 8, 2, 128, 64, -1.0, None, 0, 1), 1),  # scale < 0
+    ((A16, A16, A16, A16, A16, None, 2, 8, 2, 96, 64, 0.1, None, 0, 1), 2),    # D = 96
+    ((A16, A16 + 4, A16, A16, A16, None, 2, 8, 2, 128, 64, 0.1, None, 0, 1), 3),
+    ((A16, A16, A16, A16, A16, None, 2, 8, 2, 128, 64, 0.1, A16, 16, 1), 4),   # ws too small
+])
+def test_decode_rejects_on_host(lib, args, code):
+    assert lib.attn_decode_ex(*args, None) == code
+
+
+def test_decode_split_plan(lib):
+    # at least ~4 blocks per SM of a 152-SM part, chunks of 32..1024 keys
+    assert lib.attn_decode_chunk_len(32, 2, 4096) == 256
+    assert lib.attn_decode_chunk_len(1, 2, 4096) == 32
+    assert lib.attn_decode_chunk_len(1, 2, 0) == 0
+    for B, Hkv, L in [(1, 1, 1), (3, 2, 100), (64, 8, 32768), (1, 2, 32768)]:
+        c = lib.attn_decode_chunk_len(B, Hkv, L)
+        assert 32 <= c <= 1024 and c & (c - 1) == 0
+    ws = lib.attn_decode_workspace_bytes(32, 8, 2, 128, 4096)
+    nsplit = 4096 // 256
+    assert ws == 32 * 8 * nsplit * (128 * 4 + 8)
+    assert lib.attn_decode_workspace_bytes(2, 3, 2, 128, 10) == 0
