@@ -17,7 +17,7 @@ from __future__ import annotations
 import math
 
 from . import _lib
-from ._lib import (ATTN_BF16, ATTN_DEV_SEQLEN_CLAMPED, ATTN_DEV_WAIT_TIMEOUT, ATTN_ERR_ALIGN,
+from ._lib import (ATTN_BF16, ATTN_DEV_FP16_RANGE, ATTN_DEV_SEQLEN_CLAMPED, ATTN_DEV_WAIT_TIMEOUT, ATTN_ERR_ALIGN,
                    ATTN_ERR_CUDA, ATTN_ERR_INVALID, ATTN_ERR_TIMEOUT, ATTN_ERR_UNSUPPORTED,
                    ATTN_ERR_WORKSPACE, ATTN_F32, ATTN_OK, AttnError)
 
@@ -27,7 +27,7 @@ __all__ = [
     "attn_device_status", "attn_status_string", "attn_version", "prefill", "decode",
     "device_status", "AttnError", "ATTN_OK", "ATTN_ERR_INVALID", "ATTN_ERR_UNSUPPORTED",
     "ATTN_ERR_ALIGN", "ATTN_ERR_WORKSPACE", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "ATTN_F32",
-    "ATTN_BF16", "ATTN_DEV_SEQLEN_CLAMPED", "ATTN_DEV_WAIT_TIMEOUT", "load_library",
+    "ATTN_BF16", "ATTN_DEV_FP16_RANGE", "ATTN_DEV_SEQLEN_CLAMPED", "ATTN_DEV_WAIT_TIMEOUT", "load_library",
 ]
 
 

@@ -22,6 +22,7 @@ ATTN_F32 = 0
 ATTN_BF16 = 1
 ATTN_DEV_SEQLEN_CLAMPED = 0x1
 ATTN_DEV_WAIT_TIMEOUT = 0x2
+ATTN_DEV_FP16_RANGE = 0x4
 
 _vp = ctypes.c_void_p
 _i = ctypes.c_int

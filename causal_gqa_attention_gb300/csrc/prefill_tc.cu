@@ -7,12 +7,19 @@
 //   warp 0      TMA producer: Q tiles once, then K_j and V_j into a 2-stage ring each;
 //   warp 1      tcgen05 issuer (one thread): S_t = Q_t K_j^T into TMEM, O_t += P_t V_j with
 //               P_t read from TMEM; owns the TMEM allocation;
+//   warps 2-3   convert each landed V tile from bf16 to fp16 in place (see below);
 //   warps 4-7   softmax for tile 0, warps 8-11 for tile 1: one thread per query row (its TMEM
 //               lane). Reads the 128 scores of its row, masks, updates the running max and
-//               sum, writes P (bf16) over the scores it came from, rescales its O row when
+//               sum, writes P (fp16) over the scores it came from, rescales its O row when
 //               the max moved, and finally writes O / l and the LSE.
-// TMEM (512 columns): S_0 | S_1 | O_0 | O_1, 128 fp32 columns each; P_t is packed bf16 in the
+// TMEM (512 columns): S_0 | S_1 | O_0 | O_1, 128 fp32 columns each; P_t is packed fp16 in the
 // first 64 columns of S_t. S and P never leave the SM.
+//
+// Precision of the P V product: P is rounded to a 16-bit type before the tensor core consumes
+// it. With bf16 (8-bit significand) a peaky softmax (a few keys carrying most of the weight)
+// showed errors near 8e-3 in the output; fp16 (11-bit significand) brings that to about 1e-3.
+// The tensor core needs both operands of one product in the same type, so V is converted to
+// fp16 in shared memory; that is exact for every bf16 value with 2^-14 <= |v| <= 65280.
 //
 // The two tiles alternate on the tensor core: while tile 0's softmax runs, the tensor core
 // computes tile 1's P V and next S, and the other way round. Issue order per key tile j:
@@ -68,13 +75,20 @@ enum : int {
     B_PFULL = 11,  // 2 (per tile)
     B_OFULL = 13,  // 2 (per tile)
     B_DRAIN = 15,
-    NUM_BARS = 16
+    B_VREADY = 16,  // 2: V stage converted to fp16
+    NUM_BARS = 18
 };
 
 __device__ __forceinline__ int last_key_tile(int causal, int q_first, int nkv)
 {
     // causal: the tile whose rows start at q_first needs keys up to q_first + 127
     return causal ? min((q_first + BM - 1) / BN, nkv - 1) : nkv - 1;
+}
+
+// 1 if either bf16 half of w has magnitude >= 2^16 (beyond the fp16 range) or is inf/NaN.
+__device__ __forceinline__ uint32_t too_big_for_f16(uint32_t w)
+{
+    return (uint32_t)((w & 0x7FFF0000u) >= 0x47800000u) | (uint32_t)((w & 0x7FFFu) >= 0x4780u);
 }
 
 template <bool OUT_F32>
@@ -120,6 +134,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bar[B_OFULL + s], 1);
         }
         mbar_init(&bar[B_DRAIN], 1);
+        mbar_init(&bar[B_VREADY], 64);
+        mbar_init(&bar[B_VREADY + 1], 64);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -173,8 +189,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ================================================================ tcgen05 issuer
         if (lane == 0) {
-            constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0, 0);  // Q, K both K-major
-            constexpr uint32_t idO = idesc_bf16_f32(BM, HD, 0, 1);  // P from TMEM, V MN-major
+            constexpr uint32_t idS = idesc_f32acc(BM, BN, 0, 0, 1);  // bf16 Q, K: K-major
+            constexpr uint32_t idO = idesc_f32acc(BM, HD, 0, 1, 0);  // fp16 P (TMEM), V MN-major
             const uint32_t sQ = smem_u32(smem + kOffQ);
             const uint32_t sK = smem_u32(smem + kOffK);
             const uint32_t sV = smem_u32(smem + kOffV);
@@ -184,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool do_pv = j >= 1;
                 if (do_s && !mbar_wait(&bar[B_KFULL + (j & 1)], (j >> 1) & 1, abort_flag)) break;
                 if (do_pv &&
-                    !mbar_wait(&bar[B_VFULL + ((j - 1) & 1)], ((j - 1) >> 1) & 1, abort_flag))
+                    !mbar_wait(&bar[B_VREADY + ((j - 1) & 1)], ((j - 1) >> 1) & 1, abort_flag))
                     break;
                 tc_fence_after();
                 for (int t = 0; t < 2 && ok; ++t) {
@@ -227,6 +243,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             volatile int never = 0;
             mbar_wait(&bar[B_DRAIN], 0, &never);
         }
+    } else if (warp == 2 || warp == 3) {
+        // ================================================================ V bf16 -> fp16
+        // The P V product runs in fp16 (10-bit mantissa for P instead of bf16's 7): each V tile
+        // is converted in place once it lands, then handed to the tensor core.
+        const int ct = threadIdx.x - 64;
+        uint32_t over = 0;
+        for (int j = 0; j < n_j; ++j) {
+            const int s = j & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&bar[B_VFULL + s], (j >> 1) & 1, abort_flag)))
+                break;
+            uint4 *tile = reinterpret_cast<uint4 *>(smem + kOffV + s * kTile);
+#pragma unroll 4
+            for (int c = ct; c < (int)(kTile / 16); c += 64) {
+                uint4 w = tile[c];
+                // |bf16| >= 2^16 (magnitude bits >= 0x4780) does not fit fp16; inf, NaN too
+                over |= too_big_for_f16(w.x) | too_big_for_f16(w.y) | too_big_for_f16(w.z) |
+                        too_big_for_f16(w.w);
+                w.x = bf16x2_to_f16x2_sat(w.x);
+                w.y = bf16x2_to_f16x2_sat(w.y);
+                w.z = bf16x2_to_f16x2_sat(w.z);
+                w.w = bf16x2_to_f16x2_sat(w.w);
+                tile[c] = w;
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&bar[B_VREADY + s]);
+        }
+        if (over) atomicOr(status, 4u);
     } else if (warp >= 4) {
         // ================================================================ softmax / epilogue
         const int t = (warp - 4) / 4;
@@ -268,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float p0 = ex2(fmaf(__uint_as_float(sv[2 * c]), scale_log2, -mu));
                     const float p1 = ex2(fmaf(__uint_as_float(sv[2 * c + 1]), scale_log2, -mu));
                     rs += p0 + p1;
-                    pk[c] = pack_bf16x2(p0, p1);
+                    pk[c] = pack_f16x2(p0, p1);
                 }
                 l = fmaf(l, alpha, rs);
                 tmem_st32(tS, &pk[0]);

@@ -160,13 +160,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     return d;
 }
 
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, dense.
-// a_mn / b_mn: operand stored MN-major (1) instead of K-major (0).
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn)
+// Instruction descriptor, kind::f16: fp32 accumulator, dense; A and B both bf16 (ab = 1) or
+// both fp16 (ab = 0). a_mn / b_mn: operand stored MN-major (1) instead of K-major (0).
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, int a_mn, int b_mn, int ab)
 {
     return (1u << 4)                        // D format: fp32
-           | (1u << 7)                      // A format: bf16
-           | (1u << 10)                     // B format: bf16
+           | ((uint32_t)ab << 7)            // A format
+           | ((uint32_t)ab << 10)           // B format
            | ((uint32_t)a_mn << 15)         // A major
            | ((uint32_t)b_mn << 16)         // B major
            | ((uint32_t)(N >> 3) << 17)     // N / 8
@@ -226,6 +226,32 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// Two fp32 -> packed fp16x2 (round to nearest even); `lo` goes to the low 16 bits.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two bf16 (one 32-bit word) -> two fp16, saturating to the largest finite fp16. The result is
+// exact for 2^-14 <= |x| <= 65280 (every bf16 value there is an fp16 value).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_sat(uint32_t w)
+{
+    uint32_t r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;"
+        : "=r"(r)
+        : "f"(__uint_as_float(w & 0xFFFF0000u)), "f"(__uint_as_float(w << 16)));
+    return r;
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to the async proxy (TMA,
+// tensor cores) before a barrier arrive.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // 16-byte global load that does not allocate in L1 (streamed data).

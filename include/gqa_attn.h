@@ -62,6 +62,8 @@ typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype;
 /* Bits of the device status word (attn_device_status). */
 #define ATTN_DEV_SEQLEN_CLAMPED 0x1u /* decode: a seqlens[b] was < 0 or > max_len; clamped   */
 #define ATTN_DEV_WAIT_TIMEOUT 0x2u   /* prefill: a pipeline wait ran out; the block stopped  */
+#define ATTN_DEV_FP16_RANGE 0x4u     /* bf16 prefill: a V element beyond +-65280 (or inf/NaN) */
+                                     /* was saturated for the fp16 P V product               */
 
 /*
  * attn_prefill -- causal or non-causal prefill, bf16 in, bf16 out.
@@ -70,8 +72,9 @@ typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype;
  *   scale multiplies the scores before the softmax (usually 1/sqrt(D)).
  *   causal != 0: query i sees keys 0..i.
  * Requires Hq % Hkv == 0, D == 128, 16-byte aligned pointers.
- * Computes on tcgen05 tensor cores (bf16 products, fp32 accumulation and softmax state);
- * the probabilities are rounded to bf16 before the P V product.
+ * Computes on tcgen05 tensor cores with fp32 accumulation and fp32 softmax state: Q K^T from
+ * the bf16 inputs; P V with P rounded to fp16 and V converted bf16 -> fp16 on chip (exact for
+ * 2^-14 <= |v| <= 65280; larger |v| saturate and set ATTN_DEV_FP16_RANGE in the status word).
  */
 int attn_prefill(const void *q, const void *k, const void *v, void *o, float *lse, int B, int S,
                  int Hq, int Hkv, int D, float scale, int causal, void *stream);
