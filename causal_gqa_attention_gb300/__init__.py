@@ -22,7 +22,7 @@ from ._lib import (ATTN_BF16, ATTN_DEV_FP16_RANGE, ATTN_DEV_SEQLEN_CLAMPED, ATTN
                    ATTN_ERR_WORKSPACE, ATTN_F32, ATTN_OK, AttnError)
 
 __all__ = [
-    "attn_prefill", "attn_prefill_ex", "attn_decode", "attn_decode_ex",
+    "attn_prefill", "attn_prefill_ex", "attn_decode", "attn_decode_ex", "attn_decode_noalloc",
     "attn_decode_workspace_bytes", "attn_decode_chunk_len", "attn_reserve_workspace",
     "attn_device_status", "attn_status_string", "attn_version", "prefill", "decode",
     "device_status", "AttnError", "ATTN_OK", "ATTN_ERR_INVALID", "ATTN_ERR_UNSUPPORTED",
@@ -57,6 +57,14 @@ def attn_decode_ex(q, kcache, vcache, seqlens, o, lse, B, Hq, Hkv, D, max_len, s
                    workspace_bytes, out_dtype, stream):
     return _lib.load().attn_decode_ex(q, kcache, vcache, seqlens, o, lse, B, Hq, Hkv, D, max_len,
                                       scale, workspace, workspace_bytes, out_dtype, stream)
+
+
+def attn_decode_noalloc(q, kcache, vcache, seqlens, o, lse, B, Hq, Hkv, D, max_len, scale,
+                        out_dtype, stream):
+    """Decode that allocates nothing: scratch is a fixed array inside the library (for callers
+    that cannot call cudaMalloc). Raw pointers; returns the C status code."""
+    return _lib.load().attn_decode_noalloc(q, kcache, vcache, seqlens, o, lse, B, Hq, Hkv, D,
+                                           max_len, scale, out_dtype, stream)
 
 
 def attn_decode_workspace_bytes(B, Hq, Hkv, D, max_len):

@@ -23,6 +23,7 @@ ATTN_BF16 = 1
 ATTN_DEV_SEQLEN_CLAMPED = 0x1
 ATTN_DEV_WAIT_TIMEOUT = 0x2
 ATTN_DEV_FP16_RANGE = 0x4
+ATTN_DECODE_NOALLOC_SCRATCH_BYTES = 4 * 1024 * 1024
 
 _vp = ctypes.c_void_p
 _i = ctypes.c_int
@@ -36,6 +37,7 @@ SIGNATURES = {
     "attn_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]),
     "attn_decode_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _sz, _i,
                             _vp]),
+    "attn_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp]),
     "attn_decode_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "attn_decode_chunk_len": (_i, [_i, _i, _i]),
     "attn_reserve_workspace": (_i, [_i, _i, _i, _i, _i]),

@@ -149,6 +149,10 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CU
 
 }  // namespace
 
+namespace gqa {
+int status_word_ptr(unsigned **out) { return status_ptr(out); }
+}  // namespace gqa
+
 extern "C" {
 
 int attn_version(void) { return 100; }

@@ -44,6 +44,9 @@ struct DecodeArgs {
 };
 cudaError_t launch_decode(const DecodeArgs &a, bool out_f32, cudaStream_t stream);
 
+// Device address of the library's status word on the current device.
+int status_word_ptr(unsigned **out);
+
 // Decode work split, shared by the workspace query and the launch.
 int decode_chunk_len(int B, int Hkv, int max_len);
 size_t decode_workspace_bytes(int B, int Hq, int D, int max_len, int chunk);

@@ -119,6 +119,29 @@ int attn_decode_ex(const void *q, const void *kcache, const void *vcache, const 
                    void *o, float *lse, int B, int Hq, int Hkv, int D, int max_len, float scale,
                    void *workspace, size_t workspace_bytes, int out_dtype, void *stream);
 
+/*
+ * attn_decode_noalloc -- attn_decode_ex for callers that cannot allocate device memory.
+ * The pages describe no such variant; it exists for code that runs where cudaMalloc is not
+ * available to it: under a memory manager that owns the whole device, in a process whose
+ * allocator is frozen after start-up, or in a plug-in that is handed tensors but no allocator.
+ * It allocates nothing and takes no workspace: the per-chunk partial results go to a fixed
+ * device array of ATTN_DECODE_NOALLOC_SCRATCH_BYTES bytes inside the library, which every GPU
+ * that loads the library keeps until the process exits.
+ *   Arguments as attn_decode_ex, without workspace/workspace_bytes.
+ *   Returns ATTN_ERR_WORKSPACE when the shape's partials need more than
+ *   ATTN_DECODE_NOALLOC_SCRATCH_BYTES (attn_decode_workspace_bytes tells how much a shape
+ *   needs); nothing is launched then.
+ *   The first call on each device looks up the array's device address (with that device
+ *   current); make that first call before any stream capture.
+ *   All calls on a device share the one array and it keeps the last call's contents: calls
+ *   that overlap on the GPU (different streams, no ordering between them) race and give wrong
+ *   results. Nothing in it needs to start at zero.
+ */
+#define ATTN_DECODE_NOALLOC_SCRATCH_BYTES (4u * 1024u * 1024u)
+int attn_decode_noalloc(const void *q, const void *kcache, const void *vcache, const int *seqlens,
+                        void *o, float *lse, int B, int Hq, int Hkv, int D, int max_len,
+                        float scale, int out_dtype, void *stream);
+
 /* Workspace bytes attn_decode_ex needs for this shape (0 for invalid arguments).
  * Depends only on the arguments, not on the device. */
 size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int max_len);
