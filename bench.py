@@ -53,7 +53,21 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle sample")
-    return p.parse_args()
+    p.add_argument("--only", default="all", choices=["all", "prefill", "decode"],
+                   help="run one half of the step (profiling); the JSON line is for 'all' only")
+    p.add_argument("--prefill-batch", type=int, default=None)
+    p.add_argument("--prefill-seq", type=int, default=None)
+    p.add_argument("--decode-batch", type=int, default=None)
+    args = p.parse_args()
+    global PREFILL, DECODE
+    if args.prefill_batch or args.prefill_seq:
+        PREFILL = workloads.PrefillConfig("custom", args.prefill_batch or PREFILL.B, PREFILL.Hq,
+                                          PREFILL.Hkv, args.prefill_seq or PREFILL.S, PREFILL.D,
+                                          "bf16")
+    if args.decode_batch:
+        DECODE = workloads.DecodeConfig("custom", args.decode_batch, DECODE.Hq, DECODE.Hkv,
+                                        DECODE.D, DECODE.max_len, "uniform")
+    return args
 
 
 def peaks():
@@ -274,10 +288,12 @@ def main():
     stream = torch.cuda.current_stream(dev)
 
     def run_prefill():
-        cga.prefill(q, k, v, causal=True, out=o, lse=lse, return_lse=True)
+        if args.only != "decode":
+            cga.prefill(q, k, v, causal=True, out=o, lse=lse, return_lse=True)
 
     def run_decode():
-        cga.decode(dq, dkc, dvc, dsl, out=do)
+        if args.only != "prefill":
+            cga.decode(dq, dkc, dvc, dsl, out=do)
 
     for _ in range(args.warmup):
         run_prefill()
@@ -310,8 +326,8 @@ def main():
     pre_mean = max_over_ranks(sum(pre_ms) / len(pre_ms), world, dev)
     dec_mean = max_over_ranks(sum(dec_ms) / len(dec_ms), world, dev)
     step_ms = pre_mean + dec_mean
-    tflops = pflops / (pre_mean * 1e-3) / 1e12
-    dec_gbs = dec_bytes / (dec_mean * 1e-3) / 1e9
+    tflops = pflops / (max(pre_mean, 1e-6) * 1e-3) / 1e12
+    dec_gbs = dec_bytes / (max(dec_mean, 1e-6) * 1e-3) / 1e9
 
     # ---- end to end through the public API with host buffers
     e2e = None
@@ -363,6 +379,11 @@ def main():
         cpu = {"value": r["prefill_tflops"], "unit": "TFLOP/s", "cores": r["cores"],
                "kind": "oracle", "sample": r["sample"], "decode_gbs": r["decode_gbs"]}
 
+    if args.only != "all":
+        if rank == 0:
+            print(json.dumps({"only": args.only, "prefill_ms": pre_mean, "decode_ms": dec_mean,
+                              "prefill_tflops": tflops, "decode_gbs": dec_gbs}), flush=True)
+        return
     if rank == 0:
         peak_t = pk["bf16_tflops"]
         line = {
