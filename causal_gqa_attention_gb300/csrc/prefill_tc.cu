@@ -287,8 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 tc_fence_after();
                 uint32_t sv[128];  // raw fp32 bits of the row's scores
-#pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, &sv[c * 32]);
+                tmem_ld128(tS, sv);
                 const int k0 = j * BN;
                 if (k0 + BN > S || (causal && k0 + BN - 1 > i)) {
                     const int lim = causal ? min(i + 1, S) : S;  // keys < lim are visible
@@ -296,36 +295,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < 128; ++c)
                         if (k0 + c >= lim) sv[c] = __float_as_uint(-INFINITY);
                 }
-                float mx = __uint_as_float(sv[0]);
+                // row max: four independent chains of three-input max
+                float mc[4];
 #pragma unroll
-                for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sv[c]));
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    float a = __uint_as_float(sv[32 * q4]);
+#pragma unroll
+                    for (int e = 1; e < 31; e += 2)
+                        a = fmax3(a, __uint_as_float(sv[32 * q4 + e]),
+                                  __uint_as_float(sv[32 * q4 + e + 1]));
+                    mc[q4] = fmaxf(a, __uint_as_float(sv[32 * q4 + 31]));
+                }
+                const float mx = fmax3(mc[0], mc[1], fmaxf(mc[2], mc[3]));
                 const float m_cand = mx * scale_log2;
                 const bool need = m_cand > m_ref + kRescaleThreshold;
                 const float m_new = need ? m_cand : m_ref;
                 const float mu = (m_new == -INFINITY) ? 0.f : m_new;
                 const float alpha = ex2(m_ref - mu);
-                float rs = 0.f;
+                const float2 sc2 = make_float2(scale_log2, scale_log2);
+                const float2 nm2 = make_float2(-mu, -mu);
+                float2 rsa = make_float2(0.f, 0.f), rsb = rsa;
                 uint32_t pk[64];
 #pragma unroll
                 for (int c = 0; c < 64; ++c) {
-                    const float p0 = ex2(fmaf(__uint_as_float(sv[2 * c]), scale_log2, -mu));
-                    const float p1 = ex2(fmaf(__uint_as_float(sv[2 * c + 1]), scale_log2, -mu));
-                    rs += p0 + p1;
-                    pk[c] = pack_f16x2(p0, p1);
+                    const float2 x = ffma2(make_float2(__uint_as_float(sv[2 * c]),
+                                                       __uint_as_float(sv[2 * c + 1])),
+                                           sc2, nm2);
+                    const float2 p = make_float2(ex2(x.x), ex2(x.y));
+                    if (c & 1)
+                        rsb = fadd2(rsb, p);
+                    else
+                        rsa = fadd2(rsa, p);
+                    pk[c] = pack_f16x2(p.x, p.y);
                 }
-                l = fmaf(l, alpha, rs);
+                l = fmaf(l, alpha, (rsa.x + rsa.y) + (rsb.x + rsb.y));
                 tmem_st32(tS, &pk[0]);
                 tmem_st32(tS + 32, &pk[32]);
                 if (j > 0 && __any_sync(0xffffffffu, need)) {
-#pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t ov[32];
-                        tmem_ld32(tO + c * 32, ov);
+                    uint32_t ov[128];
+                    tmem_ld128(tO, ov);
+                    const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                        tmem_st32(tO + c * 32, ov);
+                    for (int e = 0; e < 64; ++e) {
+                        const float2 v2 = fmul2(make_float2(__uint_as_float(ov[2 * e]),
+                                                            __uint_as_float(ov[2 * e + 1])),
+                                                a2);
+                        ov[2 * e] = __float_as_uint(v2.x);
+                        ov[2 * e + 1] = __float_as_uint(v2.y);
                     }
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) tmem_st32(tO + c * 32, &ov[c * 32]);
                 }
                 tmem_st_wait();
                 tc_fence_before();
