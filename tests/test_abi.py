@@ -90,14 +90,14 @@ def test_decode_rejects_on_host(lib, args, code):
 
 
 def test_decode_split_plan(lib):
-    # at least ~4 blocks per SM of a 152-SM part, chunks of 32..1024 keys
-    assert lib.attn_decode_chunk_len(32, 2, 4096) == 256
-    assert lib.attn_decode_chunk_len(1, 2, 4096) == 32
+    # at least ~3 blocks per SM of a 152-SM part, chunks of 64..512 keys
+    assert lib.attn_decode_chunk_len(32, 2, 4096) == 512
+    assert lib.attn_decode_chunk_len(1, 2, 4096) == 64
     assert lib.attn_decode_chunk_len(1, 2, 0) == 0
     for B, Hkv, L in [(1, 1, 1), (3, 2, 100), (64, 8, 32768), (1, 2, 32768)]:
         c = lib.attn_decode_chunk_len(B, Hkv, L)
-        assert 32 <= c <= 1024 and c & (c - 1) == 0
+        assert 64 <= c <= 512 and c & (c - 1) == 0
     ws = lib.attn_decode_workspace_bytes(32, 8, 2, 128, 4096)
-    nsplit = 4096 // 256
+    nsplit = 4096 // 512
     assert ws == 32 * 8 * nsplit * (128 * 4 + 8)
     assert lib.attn_decode_workspace_bytes(2, 3, 2, 128, 10) == 0
