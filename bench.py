@@ -3,7 +3,11 @@
 One step = one pass of the whole hot path on synthetic inputs already resident in device memory:
   * prefill: B=8, Hq=8, Hkv=2, S=8192, D=128, bf16, causal (long-context throughput workload);
   * decode:  B=32, Hq=8, Hkv=2, D=128, bf16 cache, per-sequence lengths uniform in [256, 4096].
-The L2 cache is flushed (a 512 MiB memset) before each timed kernel region, outside the events.
+Before each timed kernel region the L2 cache is flushed outside the events: a 512 MiB buffer is
+written, then another 512 MiB buffer is read, so the timed kernel starts from a clean L2 (a bare
+memset would leave L2 full of dirty lines whose write-back the next kernel would pay for).
+Decode is reported twice: one call after a flush (launch latency included), and a CUDA graph of
+16 back-to-back calls over 4 rotating KV caches (together over 4x the L2), launch amortised.
 
 Printed (rank 0, one JSON line): ``value`` = prefill TFLOP/s (algorithmic causal flops over the
 measured prefill time), the decode GB/s (algorithmic bytes: every valid K/V row once, q and o)
@@ -41,6 +45,8 @@ PREFILL = workloads.CONFIGS["c5b"]
 DECODE = workloads.CONFIGS["c4b"]
 METRIC = "prefill attention TFLOP/s and decode KV-read GB/s, % of GB300 roofline"
 FLUSH_BYTES = 512 << 20
+DECODE_SETS = 4
+DECODE_CALLS = 16
 
 
 def parse():
@@ -247,7 +253,8 @@ def config_block():
                     "D": PREFILL.D, "causal": True},
         "decode": {"B": DECODE.B, "Hq": DECODE.Hq, "Hkv": DECODE.Hkv, "D": DECODE.D,
                    "max_len": DECODE.max_len, "lengths": "uniform [256, 4096]"},
-        "l2": "flushed (512 MiB memset) before every timed kernel region",
+        "l2": ("flushed before every timed kernel region (512 MiB written, then another "
+               "512 MiB read, so L2 holds no dirty lines)"),
         "parallelism": "replicas",
     }
 
@@ -283,7 +290,12 @@ def main():
     dq, dkc, dvc, dsl = dq.to(dev), dkc.to(dev), dvc.to(dev), dsl.to(dev)
     do = torch.empty_like(dq)
     cga.attn_reserve_workspace(DECODE.B, DECODE.Hq, DECODE.Hkv, DECODE.D, DECODE.max_len)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        flush_w.zero_()
+        flush_r.sum()
     pflops = workloads.prefill_flops(PREFILL.B, PREFILL.Hq, PREFILL.S, PREFILL.D, True)
     stream = torch.cuda.current_stream(dev)
 
@@ -307,11 +319,11 @@ def main():
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
     for s in range(args.steps):
-        flush.zero_()
+        flush_l2()
         ev[s][0].record(stream)
         run_prefill()
         ev[s][1].record(stream)
-        flush.zero_()
+        flush_l2()
         ev[s][2].record(stream)
         run_decode()
         ev[s][3].record(stream)
@@ -328,6 +340,42 @@ def main():
     step_ms = pre_mean + dec_mean
     tflops = pflops / (max(pre_mean, 1e-6) * 1e-3) / 1e12
     dec_gbs = dec_bytes / (max(dec_mean, 1e-6) * 1e-3) / 1e9
+
+    # ---- decode, back to back: a CUDA graph of DECODE_CALLS calls over DECODE_SETS caches
+    b2b = None
+    if args.only != "prefill":
+        sets = []
+        for k in range(DECODE_SETS):
+            tq, tkc, tvc, tsl = workloads.config_decode_inputs(DECODE, seed=100 + k, nan_fill=False)
+            nb = workloads.decode_bytes(tsl.tolist(), DECODE.Hq, DECODE.Hkv, DECODE.D)
+            sets.append((tq.to(dev), tkc.to(dev), tvc.to(dev), tsl.to(dev), nb))
+        outs = [torch.empty_like(x[0]) for x in sets]
+        for k in range(DECODE_SETS):  # warm (first-use set-up happens outside capture)
+            cga.decode(sets[k][0], sets[k][1], sets[k][2], sets[k][3], out=outs[k])
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for c in range(DECODE_CALLS):
+                k = c % DECODE_SETS
+                cga.decode(sets[k][0], sets[k][1], sets[k][2], sets[k][3], out=outs[k])
+        graph.replay()
+        torch.cuda.synchronize()
+        g_ms = []
+        for _ in range(max(3, args.steps // 2)):
+            flush_l2()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            g_ms.append(e0.elapsed_time(e1))
+        g_ms = max_over_ranks(statistics.median(g_ms), world, dev)
+        g_bytes = sum(sets[c % DECODE_SETS][4] for c in range(DECODE_CALLS))
+        b2b = {"value": g_bytes / (g_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "us_per_call": g_ms * 1e3 / DECODE_CALLS, "calls": DECODE_CALLS,
+               "cache_sets": DECODE_SETS, "frac": g_bytes / (g_ms * 1e-3) / 1e9 / pk["hbm_gbs"]}
+        del graph
 
     # ---- end to end through the public API with host buffers
     e2e = None
@@ -382,7 +430,8 @@ def main():
     if args.only != "all":
         if rank == 0:
             print(json.dumps({"only": args.only, "prefill_ms": pre_mean, "decode_ms": dec_mean,
-                              "prefill_tflops": tflops, "decode_gbs": dec_gbs}), flush=True)
+                              "prefill_tflops": tflops, "decode_gbs": dec_gbs,
+                              "decode_back_to_back": b2b}), flush=True)
         return
     if rank == 0:
         peak_t = pk["bf16_tflops"]
@@ -404,6 +453,7 @@ def main():
                         "flops": pflops, "frac_of_bf16_peak": tflops / peak_t,
                         "frac_of_bf16_sustained": tflops / pk["bf16_tflops_sustained"]},
             "decode": {"value": dec_gbs, "unit": "GB/s", "ms": dec_mean, "bytes": dec_bytes,
+                       "back_to_back": b2b,
                        "roofline": {"bound": "hbm", "achieved": dec_gbs,
                                     "peak": pk["hbm_gbs"], "unit": "GB/s",
                                     "frac": dec_gbs / pk["hbm_gbs"], "traffic": None}},

@@ -218,7 +218,7 @@ int attn_decode_chunk_len(int B, int Hkv, int max_len)
 size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int max_len)
 {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || max_len <= 0 || Hq % Hkv != 0) return 0;
-    return gqa::decode_workspace_bytes(B, Hq, D, max_len, gqa::decode_chunk_len(B, Hkv, max_len));
+    return gqa::decode_workspace_bytes(B, Hq, Hkv, D, max_len);
 }
 
 int attn_reserve_workspace(int B, int Hq, int Hkv, int D, int max_len)
@@ -236,8 +236,7 @@ int attn_decode_ex(const void *q, const void *kcache, const void *vcache, const 
     int rc = check_decode(q, kcache, vcache, seqlens, o, lse, B, Hq, Hkv, D, max_len, scale,
                           out_dtype);
     if (rc != ATTN_OK) return rc;
-    const int chunk = gqa::decode_chunk_len(B, Hkv, max_len);
-    const size_t need = gqa::decode_workspace_bytes(B, Hq, D, max_len, chunk);
+    const size_t need = gqa::decode_workspace_bytes(B, Hq, Hkv, D, max_len);
     if (workspace != nullptr) {
         if (workspace_bytes < need) return ATTN_ERR_WORKSPACE;
         if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
@@ -260,11 +259,7 @@ int attn_decode_ex(const void *q, const void *kcache, const void *vcache, const 
     a.Hkv = Hkv;
     a.D = D;
     a.max_len = max_len;
-    a.chunk = chunk;
-    a.nsplit = (max_len + chunk - 1) / chunk;
-    a.ws_o = static_cast<float *>(ws);
-    a.ws_ml = reinterpret_cast<float2 *>(static_cast<char *>(ws) +
-                                         (size_t)B * Hq * a.nsplit * D * sizeof(float));
+    a.ws = ws;
     a.scale_log2 = scale * 1.4426950408889634f;
     rc = status_ptr(&a.status);
     if (rc != ATTN_OK) return rc;

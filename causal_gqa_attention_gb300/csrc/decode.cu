@@ -54,6 +54,154 @@ struct Plan {
 // The running max per head is rescaled lazily (only when a score exceeds it by 2^8), the
 // probabilities go through shared memory to the lanes that own the V dims, and P V uses
 // packed fp32 FMAs.
+// Online-softmax update of one group's state with one stage (T keys per group, nvalid valid
+// keys in the stage). K rows of the stage first, V rows after them. Lane gl of group grp holds
+// dims gl*8 .. gl*8+7; `pw` is this group's {p, p} buffer in shared memory.
+template <int D, int HG>
+__device__ __forceinline__ void stage_update(const uint8_t *stage, int nvalid, int grp, int gl,
+                                             const float2 (&qp)[HG][4], float (&m_ref)[HG],
+                                             float2 (&acc)[HG][4],
+                                             float (&l_own)[Plan<D, HG>::NV], float2 *pw)
+{
+    using P = Plan<D, HG>;
+    constexpr int LPK = P::LPK, T = P::T, TG = P::TG, NV = P::NV, SK = P::SK;
+    // ---- partial scores for the T keys of this lane's group
+    float part[TG];
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(stage + (grp * T + t) * P::ROW + gl * 16);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        float2 kp[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) kp[e] = make_float2(bf16lo(ws[e]), bf16hi(ws[e]));
+#pragma unroll
+        for (int h = 0; h < HG; ++h) {
+            float2 d2 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) d2 = ffma2(qp[h][e], kp[e], d2);
+            part[t * HG + h] = d2.x + d2.y;
+        }
+    }
+    // ---- halving exchange across the LPK lanes of the group
+#pragma unroll
+    for (int off = LPK / 2, cur = TG; off >= 1; off >>= 1, cur >>= 1) {
+        const bool up = (gl & off) != 0;
+#pragma unroll
+        for (int e = 0; e < cur / 2; ++e) {
+            const float send = up ? part[e] : part[e + cur / 2];
+            const float keep = up ? part[e + cur / 2] : part[e];
+            part[e] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+    // part[v] is now the full score of entry gl*NV + v: key t = entry / HG, head entry % HG
+    float mv[NV];
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        const int ent = gl * NV + v;
+        const int t = ent / HG, hh = ent % HG;
+        if (grp * T + t >= nvalid) part[v] = -INFINITY;
+        float mr = m_ref[0];
+#pragma unroll
+        for (int h = 1; h < HG; ++h) mr = (hh == h) ? m_ref[h] : mr;
+        mv[v] = mr;
+    }
+    bool need = false;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) need |= part[v] > mv[v] + 8.0f;
+    if (__any_sync(0xffffffffu, need)) {
+        // exact block max per head over the group, then rescale to it
+#pragma unroll
+        for (int h = 0; h < HG; ++h) {
+            float bm = -INFINITY;
+#pragma unroll
+            for (int v = 0; v < NV; ++v)
+                if ((gl * NV + v) % HG == h) bm = fmaxf(bm, part[v]);
+#pragma unroll
+            for (int off = LPK / 2; off >= 1; off >>= 1)
+                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
+            const float mn = fmaxf(m_ref[h], bm);
+            if (mn > m_ref[h]) {
+                const float alpha = ex2(m_ref[h] - mn);  // 0 when m_ref was -inf
+                const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[h][e] = fmul2(acc[h][e], a2);
+#pragma unroll
+                for (int v = 0; v < NV; ++v)
+                    if ((gl * NV + v) % HG == h) l_own[v] *= alpha;
+                m_ref[h] = mn;
+            }
+        }
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            const int hh = (gl * NV + v) % HG;
+            float mr = m_ref[0];
+#pragma unroll
+            for (int h = 1; h < HG; ++h) mr = (hh == h) ? m_ref[h] : mr;
+            mv[v] = mr;
+        }
+    }
+    // ---- probabilities: own entries, then to shared memory for the V lanes
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        const float mu = (mv[v] == -INFINITY) ? 0.f : mv[v];
+        const float p = ex2(part[v] - mu);
+        l_own[v] += p;
+        pw[gl * NV + v] = make_float2(p, p);
+    }
+    __syncwarp();
+    // ---- O += P V for the group's keys. Rows past nvalid hold finite stale data (the ring is
+    // zeroed when the block starts and only ever receives cache rows) and get p = 0.
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(stage + SK * P::ROW +
+                                                         (grp * T + t) * P::ROW + gl * 16);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        float2 vp[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) vp[e] = make_float2(bf16lo(ws[e]), bf16hi(ws[e]));
+#pragma unroll
+        for (int h = 0; h < HG; ++h) {
+            const float2 pp = pw[t * HG + h];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[h][e] = ffma2(pp, vp[e], acc[h][e]);
+        }
+    }
+    __syncwarp();
+}
+
+// Running sums per head over the LPK lanes of a group (each lane holds the sums of its entries).
+template <int D, int HG>
+__device__ __forceinline__ void group_sums(const float (&l_own)[Plan<D, HG>::NV], int gl,
+                                           float (&lsum)[HG])
+{
+    using P = Plan<D, HG>;
+#pragma unroll
+    for (int h = 0; h < HG; ++h) {
+        float x = 0.f;
+#pragma unroll
+        for (int v = 0; v < P::NV; ++v)
+            if ((gl * P::NV + v) % HG == h) x += l_own[v];
+#pragma unroll
+        for (int off = P::LPK / 2; off >= 1; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+        lsum[h] = x;
+    }
+}
+
+// q fragment (8 dims of each of the HG heads starting at h0), scaled to log2 units.
+template <int D, int HG>
+__device__ __forceinline__ void load_q(const __nv_bfloat16 *q, size_t row0, int gl,
+                                       float scale_log2, float2 (&qp)[HG][4])
+{
+#pragma unroll
+    for (int h = 0; h < HG; ++h) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(q + (row0 + h) * D + gl * 8);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            qp[h][e] = make_float2(bf16lo(ws[e]) * scale_log2, bf16hi(ws[e]) * scale_log2);
+    }
+}
+
 template <int D, int HG>
 __global__ void __launch_bounds__(kWarps * 32)
     decode_split_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ kc,
@@ -63,7 +211,7 @@ __global__ void __launch_bounds__(kWarps * 32)
                         unsigned *__restrict__ status)
 {
     using P = Plan<D, HG>;
-    constexpr int LPK = P::LPK, GPW = P::GPW, T = P::T, TG = P::TG, NV = P::NV, SK = P::SK;
+    constexpr int LPK = P::LPK, GPW = P::GPW, T = P::T, NV = P::NV, SK = P::SK;
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *ring = smem;
     float2 *pbuf = reinterpret_cast<float2 *>(smem + (P::RING > P::COMB ? P::RING : P::COMB));
@@ -90,6 +238,9 @@ __global__ void __launch_bounds__(kWarps * 32)
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int grp = lane / LPK, gl = lane % LPK;
 
+    for (int i = threadIdx.x; i < P::RING / 16; i += kWarps * 32)
+        reinterpret_cast<uint4 *>(ring)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
     if (threadIdx.x == 0) {
         for (int i = 0; i < kWarps * kRing; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
@@ -113,16 +264,8 @@ __global__ void __launch_bounds__(kWarps * 32)
         for (int r = 0; r < kRing; ++r)
             if (warp + r * kWarps < nstage) issue(warp + r * kWarps);
 
-    // query fragments (8 dims of each head), scaled so scores come out in log2 units
     float2 qp[HG][4];
-#pragma unroll
-    for (int h = 0; h < HG; ++h) {
-        const uint4 w = *reinterpret_cast<const uint4 *>(q + ((size_t)b * Hq + h0 + h) * D + gl * 8);
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            qp[h][e] = make_float2(bf16lo(ws[e]) * scale_log2, bf16hi(ws[e]) * scale_log2);
-    }
+    load_q<D, HG>(q, (size_t)b * Hq + h0, gl, scale_log2, qp);
 
     float m_ref[HG];       // running max reference per head (uniform over the group)
     float2 acc[HG][4];     // unnormalised output, this lane's 8 dims of each head
@@ -147,110 +290,8 @@ __global__ void __launch_bounds__(kWarps * 32)
         const int k0 = start + i * SK;
         const int nvalid = min(SK, end - k0);
 
-        // ---- partial scores for the T keys of this lane's group
-        float part[TG];
-#pragma unroll
-        for (int t = 0; t < T; ++t) {
-            const uint4 w = *reinterpret_cast<const uint4 *>(stage + (grp * T + t) * P::ROW + gl * 16);
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-            float2 kp[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) kp[e] = make_float2(bf16lo(ws[e]), bf16hi(ws[e]));
-#pragma unroll
-            for (int h = 0; h < HG; ++h) {
-                float2 d2 = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) d2 = ffma2(qp[h][e], kp[e], d2);
-                part[t * HG + h] = d2.x + d2.y;
-            }
-        }
-        // ---- halving exchange across the LPK lanes of the group
-#pragma unroll
-        for (int off = LPK / 2, cur = TG; off >= 1; off >>= 1, cur >>= 1) {
-            const bool up = (gl & off) != 0;
-#pragma unroll
-            for (int e = 0; e < cur / 2; ++e) {
-                const float send = up ? part[e] : part[e + cur / 2];
-                const float keep = up ? part[e + cur / 2] : part[e];
-                part[e] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-            }
-        }
-        // part[v] is now the full score of entry gl*NV + v: key t = entry / HG, head entry % HG
-        float mv[NV];
-#pragma unroll
-        for (int v = 0; v < NV; ++v) {
-            const int ent = gl * NV + v;
-            const int t = ent / HG, hh = ent % HG;
-            if (grp * T + t >= nvalid) part[v] = -INFINITY;
-            float mr = m_ref[0];
-#pragma unroll
-            for (int h = 1; h < HG; ++h) mr = (hh == h) ? m_ref[h] : mr;
-            mv[v] = mr;
-        }
-        bool need = false;
-#pragma unroll
-        for (int v = 0; v < NV; ++v) need |= part[v] > mv[v] + 8.0f;
-        if (__any_sync(0xffffffffu, need)) {
-            // exact block max per head over the group, then rescale to it
-#pragma unroll
-            for (int h = 0; h < HG; ++h) {
-                float bm = -INFINITY;
-#pragma unroll
-                for (int v = 0; v < NV; ++v)
-                    if ((gl * NV + v) % HG == h) bm = fmaxf(bm, part[v]);
-#pragma unroll
-                for (int off = LPK / 2; off >= 1; off >>= 1)
-                    bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
-                const float mn = fmaxf(m_ref[h], bm);
-                if (mn > m_ref[h]) {
-                    const float alpha = ex2(m_ref[h] - mn);  // 0 when m_ref was -inf
-                    const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) acc[h][e] = fmul2(acc[h][e], a2);
-#pragma unroll
-                    for (int v = 0; v < NV; ++v)
-                        if ((gl * NV + v) % HG == h) l_own[v] *= alpha;
-                    m_ref[h] = mn;
-                }
-            }
-#pragma unroll
-            for (int v = 0; v < NV; ++v) {
-                const int hh = (gl * NV + v) % HG;
-                float mr = m_ref[0];
-#pragma unroll
-                for (int h = 1; h < HG; ++h) mr = (hh == h) ? m_ref[h] : mr;
-                mv[v] = mr;
-            }
-        }
-        // ---- probabilities: own entries, then to shared memory for the V lanes
-        float2 *pw = pbuf + (warp * GPW + grp) * T * HG;
-#pragma unroll
-        for (int v = 0; v < NV; ++v) {
-            const float mu = (mv[v] == -INFINITY) ? 0.f : mv[v];
-            const float p = ex2(part[v] - mu);
-            l_own[v] += p;
-            pw[gl * NV + v] = make_float2(p, p);
-        }
-        __syncwarp();
-        // ---- O += P V for the group's keys
-#pragma unroll
-        for (int t = 0; t < T; ++t) {
-            if (grp * T + t < nvalid) {
-                const uint4 w = *reinterpret_cast<const uint4 *>(stage + SK * P::ROW +
-                                                                 (grp * T + t) * P::ROW + gl * 16);
-                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-                float2 vp[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) vp[e] = make_float2(bf16lo(ws[e]), bf16hi(ws[e]));
-#pragma unroll
-                for (int h = 0; h < HG; ++h) {
-                    const float2 pp = pw[t * HG + h];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) acc[h][e] = ffma2(pp, vp[e], acc[h][e]);
-                }
-            }
-        }
-        __syncwarp();
+        stage_update<D, HG>(stage, nvalid, grp, gl, qp, m_ref, acc, l_own,
+                            pbuf + (warp * GPW + grp) * T * HG);
         if (lane == 0 && i + kRing * kWarps < nstage) {
             fence_proxy_async_smem();
             issue(i + kRing * kWarps);
@@ -265,18 +306,8 @@ __global__ void __launch_bounds__(kWarps * 32)
         }
     }
 
-    // ---- running sums per head over the group's lanes
     float lsum[HG];
-#pragma unroll
-    for (int h = 0; h < HG; ++h) {
-        float x = 0.f;
-#pragma unroll
-        for (int v = 0; v < NV; ++v)
-            if ((gl * NV + v) % HG == h) x += l_own[v];
-#pragma unroll
-        for (int off = LPK / 2; off >= 1; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-        lsum[h] = x;
-    }
+    group_sums<D, HG>(l_own, gl, lsum);
     __syncthreads();  // every warp done with the ring: reuse it for the combine
     // comb layout: [state = warp*GPW + grp][h][D + 2]: D outputs, then m and l
     const int st = warp * GPW + grp;
@@ -313,6 +344,339 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
     // the merge kernel may start launching once every block got here (or exited)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ stream split (B <= 1024)
+
+constexpr int kStreamMaxWarps = 1824;  // 152 SMs x 3 resident blocks x 4 warps
+constexpr int kStreamMinKeys = 64;     // smallest slice of keys a warp is given
+constexpr int kStreamMaxBatch = 1024;  // larger batches use the chunked kernel
+
+__device__ __forceinline__ int clamp_len(int L, int max_len)
+{
+    return L < 0 ? 0 : (L > max_len ? max_len : L);
+}
+
+// Sum over b in [0, nb) of clamp(seqlens[b]), over the warp (every lane gets the total).
+__device__ __forceinline__ long long warp_len_sum(const int *seqlens, int nb, int max_len, int lane)
+{
+    long long x = 0;
+    for (int b = lane; b < nb; b += 32) x += clamp_len(seqlens[b], max_len);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    return x;
+}
+
+// The keys of all sequences and all (kv head, query-head subgroup) streams form one list:
+// sequence b, stream s_local (NGS per sequence), key j at position
+//   NGS * sum_{b' < b} L_b' + s_local * L_b + j.
+// Warp W of the NWT warps of the grid takes positions [W*KP, W*KP + KP) with
+// KP = max(ceil(total / NWT), kStreamMinKeys): every warp moves the same number of bytes.
+// Where a slice crosses a stream boundary it produces one partial per piece; piece
+// (warp W, stream s = b*NGS + s_local) is stored at index W + s (unique, since both grow
+// along the list), so the merge finds the pieces of a stream as a contiguous range of warps.
+__device__ __forceinline__ long long stream_slice(long long total, int nwt)
+{
+    const long long kp = (total + nwt - 1) / nwt;
+    return kp > kStreamMinKeys ? kp : (long long)kStreamMinKeys;
+}
+
+struct StreamCursor {
+    long long pos;  // list position of the next key
+    int b, sl, off, Lb;
+};
+
+__device__ __forceinline__ void cursor_advance(StreamCursor &c, int n, const int *seqlens, int B,
+                                               int max_len, int NGS)
+{
+    c.pos += n;
+    c.off += n;
+    if (c.off == c.Lb) {
+        c.off = 0;
+        if (++c.sl == NGS) {
+            c.sl = 0;
+            do {
+                ++c.b;
+                c.Lb = c.b < B ? clamp_len(seqlens[c.b], max_len) : 0;
+            } while (c.b < B && c.Lb == 0);
+        }
+    }
+}
+
+template <int D, int HG>
+__global__ void __launch_bounds__(kWarps * 32)
+    decode_stream_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ kc,
+                         const __nv_bfloat16 *__restrict__ vc, const int *__restrict__ seqlens,
+                         float *__restrict__ ws_o, float2 *__restrict__ ws_ml, int B, int Hq,
+                         int Hkv, int max_len, float scale_log2, unsigned *__restrict__ status)
+{
+    using P = Plan<D, HG>;
+    constexpr int LPK = P::LPK, GPW = P::GPW, T = P::T, NV = P::NV, SK = P::SK;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t *ring = smem;
+    float2 *pbuf = reinterpret_cast<float2 *>(smem + P::RING);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + P::RING + P::PBUF);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int grp = lane / LPK, gl = lane % LPK;
+    const int G = Hq / Hkv, SUB = G / HG, NGS = Hkv * SUB;
+    const int W = blockIdx.x * kWarps + warp, NWT = gridDim.x * kWarps;
+
+    for (int i = threadIdx.x; i < P::RING / 16; i += kWarps * 32)
+        reinterpret_cast<uint4 *>(ring)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kWarps * kRing; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // ---- this warp's slice of the key list
+    bool bad = false;
+    for (int b = lane; b < B; b += 32) {
+        const int L = seqlens[b];
+        bad |= (L < 0 || L > max_len);
+    }
+    if (__any_sync(0xffffffffu, bad) && W == 0 && lane == 0) atomicOr(status, 1u);
+    const long long total = warp_len_sum(seqlens, B, max_len, lane) * NGS;
+    const long long KP = stream_slice(total, NWT);
+    const long long r0 = (long long)W * KP;
+    const long long r1 = r0 + KP < total ? r0 + KP : total;
+    if (r0 < total) {
+        // sequence holding position r0: scan the per-sequence list lengths 32 at a time
+        long long base = 0;
+        int b = 0;
+        for (int b0 = 0;; b0 += 32) {
+            const int bb = b0 + lane;
+            const long long x = bb < B ? (long long)clamp_len(seqlens[bb], max_len) * NGS : 0;
+            long long incl = x;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const long long y = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += y;
+            }
+            const long long tot32 = __shfl_sync(0xffffffffu, incl, 31);
+            if (r0 < base + tot32) {
+                const unsigned m = __ballot_sync(0xffffffffu, base + incl > r0);
+                const int j = __ffs(m) - 1;
+                b = b0 + j;
+                base += __shfl_sync(0xffffffffu, incl - x, j);
+                break;
+            }
+            base += tot32;
+        }
+        StreamCursor c0;
+        c0.pos = r0;
+        c0.b = b;
+        c0.Lb = clamp_len(seqlens[b], max_len);
+        const long long rel = r0 - base;
+        c0.sl = (int)(rel / c0.Lb);
+        c0.off = (int)(rel % c0.Lb);
+
+        // ---- producer side (lane 0 issues; every lane tracks the cursor)
+        StreamCursor pc = c0;
+        int issued = 0;
+        auto issue_next = [&]() {
+            if (pc.pos >= r1) return;
+            const long long left_piece = (long long)(pc.Lb - pc.off);
+            const long long left_slice = r1 - pc.pos;
+            const int n = (int)min((long long)SK, min(left_piece, left_slice));
+            if (lane == 0) {
+                const int g = pc.sl / SUB;
+                const size_t row = ((size_t)pc.b * Hkv + g) * (size_t)max_len + pc.off;
+                const int slot = issued % kRing;
+                uint8_t *dst = ring + (warp * kRing + slot) * P::STAGE;
+                uint64_t *bar = &bars[warp * kRing + slot];
+                mbar_arrive_expect_tx(bar, 2u * n * P::ROW);
+                bulk_load(dst, kc + row * D, n * P::ROW, bar);
+                bulk_load(dst + SK * P::ROW, vc + row * D, n * P::ROW, bar);
+            }
+            cursor_advance(pc, n, seqlens, B, max_len, NGS);
+            ++issued;
+        };
+        for (int r = 0; r < kRing; ++r) issue_next();
+
+        // ---- consumer side
+        StreamCursor cc = c0;
+        float2 qp[HG][4];
+        float m_ref[HG];
+        float2 acc[HG][4];
+        float l_own[NV];
+        float2 *pw = pbuf + (warp * GPW + grp) * T * HG;
+        volatile int never = 0;
+        int it = 0;
+        bool ok = true;
+        while (cc.pos < r1) {
+            const int n = (int)min((long long)SK, min((long long)(cc.Lb - cc.off), r1 - cc.pos));
+            const bool first = (cc.pos == r0) || (cc.off == 0);
+            const bool last = (cc.off + n == cc.Lb) || (cc.pos + n == r1);
+            if (first) {
+                const int g = cc.sl / SUB, gs = cc.sl % SUB;
+                load_q<D, HG>(q, (size_t)cc.b * Hq + g * G + gs * HG, gl, scale_log2, qp);
+#pragma unroll
+                for (int h = 0; h < HG; ++h) {
+                    m_ref[h] = -INFINITY;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[h][e] = make_float2(0.f, 0.f);
+                }
+#pragma unroll
+                for (int v = 0; v < NV; ++v) l_own[v] = 0.f;
+            }
+            const int slot = it % kRing;
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(&bars[warp * kRing + slot], (it / kRing) & 1, &never));
+            if (!ok) break;
+            stage_update<D, HG>(ring + (warp * kRing + slot) * P::STAGE, n, grp, gl, qp, m_ref,
+                                acc, l_own, pw);
+            if (last) {
+                float lsum[HG];
+                group_sums<D, HG>(l_own, gl, lsum);
+                // combine the GPW groups of the warp (lanes gl, gl + LPK, ...)
+#pragma unroll
+                for (int off = LPK; off < 32; off <<= 1) {
+#pragma unroll
+                    for (int h = 0; h < HG; ++h) {
+                        const float mo = __shfl_xor_sync(0xffffffffu, m_ref[h], off);
+                        const float mn = fmaxf(m_ref[h], mo);
+                        const float mu = (mn == -INFINITY) ? 0.f : mn;
+                        const float a = ex2(m_ref[h] - mu);
+                        lsum[h] *= a;
+                        lsum[h] += __shfl_xor_sync(0xffffffffu, lsum[h], off);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            acc[h][e] = fmul2(acc[h][e], make_float2(a, a));
+                            acc[h][e].x += __shfl_xor_sync(0xffffffffu, acc[h][e].x, off);
+                            acc[h][e].y += __shfl_xor_sync(0xffffffffu, acc[h][e].y, off);
+                        }
+                        m_ref[h] = mn;
+                    }
+                }
+                if (grp == 0) {
+                    const size_t piece = (size_t)W + (size_t)cc.b * NGS + cc.sl;
+#pragma unroll
+                    for (int h = 0; h < HG; ++h) {
+                        float4 *dst = reinterpret_cast<float4 *>(ws_o + (piece * HG + h) * D + gl * 8);
+                        dst[0] = make_float4(acc[h][0].x, acc[h][0].y, acc[h][1].x, acc[h][1].y);
+                        dst[1] = make_float4(acc[h][2].x, acc[h][2].y, acc[h][3].x, acc[h][3].y);
+                        if (gl == 0) ws_ml[piece * HG + h] = make_float2(m_ref[h], lsum[h]);
+                    }
+                }
+            }
+            if (lane == 0) fence_proxy_async_smem();
+            __syncwarp();
+            issue_next();
+            cursor_advance(cc, n, seqlens, B, max_len, NGS);
+            ++it;
+        }
+        if (!ok) {
+            if (lane == 0) atomicOr(status, 2u);
+            for (int r = it; r < issued; ++r)
+                mbar_wait(&bars[warp * kRing + r % kRing], (r / kRing) & 1, &never);
+        }
+    }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Merge for the stream kernel: one block per (sequence, query head). Warp w combines pieces
+// w, w + 4, ... (in order), all its loads issued together; the four warp results are then
+// combined in warp order through shared memory, so the result does not depend on timing.
+template <bool OUT_F32, int D, int HG>
+__global__ void __launch_bounds__(128)
+    decode_stream_merge_kernel(const float *__restrict__ ws_o, const float2 *__restrict__ ws_ml,
+                               const int *__restrict__ seqlens, void *__restrict__ o,
+                               float *__restrict__ lse, int B, int Hq, int Hkv, int max_len,
+                               int nwt)
+{
+    constexpr int DL = D / 32;
+    constexpr int PW = 8;  // pieces per warp per round
+    __shared__ float s_acc[4][D];
+    __shared__ float s_m[4], s_l[4];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int bh = blockIdx.x;
+    const int b = bh / Hq, h = bh % Hq;
+    const int G = Hq / Hkv, SUB = G / HG, NGS = Hkv * SUB;
+    const int g = h / G, gs = (h % G) / HG, hl = (h % G) % HG;
+    const int sl = g * SUB + gs;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const long long total = warp_len_sum(seqlens, B, max_len, lane) * NGS;
+    const long long base = warp_len_sum(seqlens, b, max_len, lane) * NGS;
+    const long long KP = stream_slice(total, nwt);
+    const int Lb = clamp_len(seqlens[b], max_len);
+    const long long start = base + (long long)sl * Lb;
+    const int wf = (int)(start / KP);
+    const int n = Lb > 0 ? (int)((start + Lb - 1) / KP) - wf + 1 : 0;
+    const size_t row0 = ((size_t)wf + (size_t)b * NGS + sl) * HG + hl;  // piece j: row0 + j*HG
+
+    float M = -INFINITY, Ls = 0.f, acc[DL];
+#pragma unroll
+    for (int e = 0; e < DL; ++e) acc[e] = 0.f;
+    for (int j0 = warp; j0 < n; j0 += 4 * PW) {
+        float2 mlj[PW];
+        float x[PW][DL];
+#pragma unroll
+        for (int k = 0; k < PW; ++k) {
+            const int j = j0 + 4 * k;
+            if (j < n) {
+                const size_t row = row0 + (size_t)j * HG;
+                mlj[k] = ws_ml[row];
+                const float *src = ws_o + row * D + lane * DL;
+#pragma unroll
+                for (int e = 0; e < DL; ++e) x[k][e] = src[e];
+            } else {
+                mlj[k] = make_float2(-INFINITY, 0.f);
+#pragma unroll
+                for (int e = 0; e < DL; ++e) x[k][e] = 0.f;
+            }
+        }
+        float cm = M;
+#pragma unroll
+        for (int k = 0; k < PW; ++k) cm = fmaxf(cm, mlj[k].x);
+        const float Mu = (cm == -INFINITY) ? 0.f : cm;
+        const float a = ex2(M - Mu);
+        Ls *= a;
+#pragma unroll
+        for (int e = 0; e < DL; ++e) acc[e] *= a;
+#pragma unroll
+        for (int k = 0; k < PW; ++k) {
+            const float w = ex2(mlj[k].x - Mu);
+            Ls = fmaf(w, mlj[k].y, Ls);
+#pragma unroll
+            for (int e = 0; e < DL; ++e) acc[e] = fmaf(w, x[k][e], acc[e]);
+        }
+        M = cm;
+    }
+#pragma unroll
+    for (int e = 0; e < DL; ++e) s_acc[warp][lane * DL + e] = acc[e];
+    if (lane == 0) {
+        s_m[warp] = M;
+        s_l[warp] = Ls;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        float Mt = fmaxf(fmaxf(s_m[0], s_m[1]), fmaxf(s_m[2], s_m[3]));
+        const float Mu = (Mt == -INFINITY) ? 0.f : Mt;
+        float Lt = 0.f, r[DL];
+#pragma unroll
+        for (int e = 0; e < DL; ++e) r[e] = 0.f;
+#pragma unroll
+        for (int w2 = 0; w2 < 4; ++w2) {
+            const float wgt = ex2(s_m[w2] - Mu);
+            Lt = fmaf(wgt, s_l[w2], Lt);
+#pragma unroll
+            for (int e = 0; e < DL; ++e) r[e] = fmaf(wgt, s_acc[w2][lane * DL + e], r[e]);
+        }
+        const float inv = (n > 0 && Lt > 0.f) ? 1.f / Lt : 0.f;
+#pragma unroll
+        for (int e = 0; e < DL; ++e) {
+            const float v = r[e] * inv;
+            if (OUT_F32)
+                static_cast<float *>(o)[(size_t)bh * D + lane * DL + e] = v;
+            else
+                static_cast<__nv_bfloat16 *>(o)[(size_t)bh * D + lane * DL + e] = __float2bfloat16_rn(v);
+        }
+        if (lse != nullptr && lane == 0)
+            lse[bh] = (n > 0 && Lt > 0.f) ? (Mt + log2f(Lt)) * 0.69314718055994531f : -INFINITY;
+    }
 }
 
 constexpr int kMergeWarps = 4;  // (sequence, query head) rows per merge block, one per warp
@@ -440,22 +804,94 @@ cudaError_t launch_split_t(const DecodeArgs &a, cudaStream_t st)
     return cudaGetLastError();
 }
 
+int largest_group(int G)
+{
+    return G % 8 == 0 ? 8 : (G % 4 == 0 ? 4 : (G % 2 == 0 ? 2 : 1));
+}
+
+template <int D, int HG>
+cudaError_t launch_stream_t(const DecodeArgs &a, bool out_f32, cudaStream_t st)
+{
+    using P = Plan<D, HG>;
+    static bool attr_set[64] = {};
+    static int blocks_cached[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    int blocks = dev < 64 ? blocks_cached[dev] : 0;
+    if (dev >= 64 || !attr_set[dev]) {
+        e = cudaFuncSetAttribute(decode_stream_kernel<D, HG>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, P::RING + P::PBUF + P::BARS);
+        if (e != cudaSuccess) return e;
+        int sms = 0, occ = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_stream_kernel<D, HG>,
+                                                          kWarps * 32, P::RING + P::PBUF + P::BARS);
+        if (e != cudaSuccess) return e;
+        blocks = sms * (occ > 0 ? occ : 1);
+        if (blocks * kWarps > kStreamMaxWarps) blocks = kStreamMaxWarps / kWarps;
+        if (dev < 64) {
+            blocks_cached[dev] = blocks;
+            attr_set[dev] = true;
+        }
+    }
+    float *ws_o = static_cast<float *>(a.ws);
+    const size_t rows = (size_t)kStreamMaxWarps * HG + (size_t)a.B * a.Hq;
+    float2 *ws_ml = reinterpret_cast<float2 *>(ws_o + rows * D);
+    decode_stream_kernel<D, HG><<<blocks, kWarps * 32, P::RING + P::PBUF + P::BARS, st>>>(
+        static_cast<const __nv_bfloat16 *>(a.q), static_cast<const __nv_bfloat16 *>(a.kc),
+        static_cast<const __nv_bfloat16 *>(a.vc), a.seqlens, ws_o, ws_ml, a.B, a.Hq, a.Hkv,
+        a.max_len, a.scale_log2, a.status);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.B * a.Hq);
+    cfg.blockDim = dim3(128);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int nwt = blocks * kWarps;
+    if (out_f32)
+        return cudaLaunchKernelEx(&cfg, decode_stream_merge_kernel<true, D, HG>, (const float *)ws_o,
+                                  (const float2 *)ws_ml, a.seqlens, a.o, a.lse, a.B, a.Hq, a.Hkv,
+                                  a.max_len, nwt);
+    return cudaLaunchKernelEx(&cfg, decode_stream_merge_kernel<false, D, HG>, (const float *)ws_o,
+                              (const float2 *)ws_ml, a.seqlens, a.o, a.lse, a.B, a.Hq, a.Hkv,
+                              a.max_len, nwt);
+}
+
+template <int D>
+cudaError_t launch_stream_d(const DecodeArgs &a, bool out_f32, cudaStream_t st)
+{
+    switch (largest_group(a.Hq / a.Hkv)) {
+    case 8: return launch_stream_t<D, 8>(a, out_f32, st);
+    case 4: return launch_stream_t<D, 4>(a, out_f32, st);
+    case 2: return launch_stream_t<D, 2>(a, out_f32, st);
+    default: return launch_stream_t<D, 1>(a, out_f32, st);
+    }
+}
+
 template <int D>
 cudaError_t launch_split_d(const DecodeArgs &a, cudaStream_t st)
 {
-    const int G = a.Hq / a.Hkv;
-    if (G % 8 == 0) return launch_split_t<D, 8>(a, st);
-    if (G % 4 == 0) return launch_split_t<D, 4>(a, st);
-    if (G % 2 == 0) return launch_split_t<D, 2>(a, st);
-    return launch_split_t<D, 1>(a, st);
+    switch (largest_group(a.Hq / a.Hkv)) {
+    case 8: return launch_split_t<D, 8>(a, st);
+    case 4: return launch_split_t<D, 4>(a, st);
+    case 2: return launch_split_t<D, 2>(a, st);
+    default: return launch_split_t<D, 1>(a, st);
+    }
 }
 
 }  // namespace
 
 int decode_chunk_len(int B, int Hkv, int max_len)
 {
-    // Aim for about three blocks per SM on a 152-SM GB300 at the shape's largest length;
-    // chunks stay between 64 and 512 keys (at least one stage per warp of a block).
+    // Chunked kernel (batches above the stream kernel's limit): aim for about three blocks per
+    // SM of a 152-SM GB300 at the shape's largest length; chunks of 64 to 512 keys.
     const long long target = 3LL * 152;
     int chunk = 512;
     while (chunk > 64 &&
@@ -464,23 +900,35 @@ int decode_chunk_len(int B, int Hkv, int max_len)
     return chunk;
 }
 
-size_t decode_workspace_bytes(int B, int Hq, int D, int max_len, int chunk)
+size_t decode_workspace_bytes(int B, int Hq, int Hkv, int D, int max_len)
 {
+    if (B <= kStreamMaxBatch) {
+        const size_t HG = (size_t)largest_group(Hq / Hkv);
+        const size_t rows = (size_t)kStreamMaxWarps * HG + (size_t)B * Hq;
+        return rows * D * sizeof(float) + rows * sizeof(float2);
+    }
+    const int chunk = decode_chunk_len(B, Hkv, max_len);
     const size_t nsplit = ((size_t)max_len + chunk - 1) / chunk;
     const size_t rows = (size_t)B * Hq * nsplit;
     return rows * D * sizeof(float) + rows * sizeof(float2);
 }
 
-cudaError_t launch_decode(const DecodeArgs &a, bool out_f32, cudaStream_t st)
+cudaError_t launch_decode(const DecodeArgs &a0, bool out_f32, cudaStream_t st)
 {
+    DecodeArgs a = a0;
+    if (a.B <= kStreamMaxBatch)
+        return a.D == 128 ? launch_stream_d<128>(a, out_f32, st) : launch_stream_d<64>(a, out_f32, st);
+    a.chunk = decode_chunk_len(a.B, a.Hkv, a.max_len);
+    a.nsplit = (a.max_len + a.chunk - 1) / a.chunk;
+    a.ws_o = static_cast<float *>(a.ws);
+    a.ws_ml = reinterpret_cast<float2 *>(a.ws_o + (size_t)a.B * a.Hq * a.nsplit * a.D);
     cudaError_t e = (a.D == 128) ? launch_split_d<128>(a, st) : launch_split_d<64>(a, st);
     if (e != cudaSuccess) return e;
     if (a.D == 128)
         e = out_f32 ? launch_merge<true, 128>(a, st) : launch_merge<false, 128>(a, st);
     else
         e = out_f32 ? launch_merge<true, 64>(a, st) : launch_merge<false, 64>(a, st);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace gqa

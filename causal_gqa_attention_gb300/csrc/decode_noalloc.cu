@@ -66,8 +66,7 @@ extern "C" int attn_decode_noalloc(const void *q, const void *kcache, const void
         return ATTN_ERR_ALIGN;
     if (!aligned4(seqlens) || (lse && !aligned4(lse))) return ATTN_ERR_ALIGN;
 
-    const int chunk = gqa::decode_chunk_len(B, Hkv, max_len);
-    const size_t need = gqa::decode_workspace_bytes(B, Hq, D, max_len, chunk);
+    const size_t need = gqa::decode_workspace_bytes(B, Hq, Hkv, D, max_len);
     if (need > (size_t)ATTN_DECODE_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_WORKSPACE;
 
     void *ws = nullptr;
@@ -85,13 +84,9 @@ extern "C" int attn_decode_noalloc(const void *q, const void *kcache, const void
     a.Hkv = Hkv;
     a.D = D;
     a.max_len = max_len;
-    a.chunk = chunk;
-    a.nsplit = (max_len + chunk - 1) / chunk;
-    // No slot needs clearing: the merge kernel reads only the chunks that the split kernel of
-    // the same call wrote.
-    a.ws_o = static_cast<float *>(ws);
-    a.ws_ml = reinterpret_cast<float2 *>(static_cast<char *>(ws) +
-                                         (size_t)B * Hq * a.nsplit * D * sizeof(float));
+    // Nothing needs clearing: every partial result the merge kernel reads was written by the
+    // split kernel of the same call.
+    a.ws = ws;
     a.scale_log2 = scale * 1.4426950408889634f;
     rc = gqa::status_word_ptr(&a.status);
     if (rc != ATTN_OK) return rc;

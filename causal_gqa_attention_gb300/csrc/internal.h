@@ -28,19 +28,23 @@ cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, f
                                float *lse, int B, int S, int Hq, int Hkv, int D, float scale,
                                int causal, cudaStream_t stream);
 
-// Decode: split kernel over (chunk, kv head [, query-head subgroup], batch) writing partial
-// (m, l, o) per chunk into the workspace, then the merge kernel.
+// Decode: a split kernel writes partial (m, l, o) results to the workspace and a merge kernel
+// combines them. Batches up to 1024 use the stream kernel (every warp of a persistent grid
+// takes an equal slice of all keys), larger ones the chunked kernel (one block per key chunk).
 struct DecodeArgs {
     const void *q;        // [B, Hq, D] bf16
     const void *kc, *vc;  // [B, Hkv, max_len, D] bf16
     const int *seqlens;   // [B]
     void *o;              // [B, Hq, D] bf16 or fp32
     float *lse;           // [B, Hq] or nullptr
-    float *ws_o;          // [B, Hq, nsplit, D]
-    float2 *ws_ml;        // [B, Hq, nsplit]: (max in log2 units, sum)
-    int B, Hq, Hkv, D, max_len, chunk, nsplit;
+    void *ws;             // decode_workspace_bytes(...) bytes, 16-byte aligned
+    int B, Hq, Hkv, D, max_len;
     float scale_log2;
     unsigned *status;
+    // filled in by launch_decode for the chunked kernel
+    float *ws_o = nullptr;
+    float2 *ws_ml = nullptr;
+    int chunk = 0, nsplit = 0;
 };
 cudaError_t launch_decode(const DecodeArgs &a, bool out_f32, cudaStream_t stream);
 
@@ -49,6 +53,6 @@ int status_word_ptr(unsigned **out);
 
 // Decode work split, shared by the workspace query and the launch.
 int decode_chunk_len(int B, int Hkv, int max_len);
-size_t decode_workspace_bytes(int B, int Hq, int D, int max_len, int chunk);
+size_t decode_workspace_bytes(int B, int Hq, int Hkv, int D, int max_len);
 
 }  // namespace gqa

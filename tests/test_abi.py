@@ -97,7 +97,11 @@ def test_decode_split_plan(lib):
     for B, Hkv, L in [(1, 1, 1), (3, 2, 100), (64, 8, 32768), (1, 2, 32768)]:
         c = lib.attn_decode_chunk_len(B, Hkv, L)
         assert 64 <= c <= 512 and c & (c - 1) == 0
+    # batches up to 1024: stream kernel, partials for 1824 warp slices x 4 heads + one per
+    # (sequence, head); larger batches: one partial per (sequence, head, chunk)
     ws = lib.attn_decode_workspace_bytes(32, 8, 2, 128, 4096)
-    nsplit = 4096 // 512
-    assert ws == 32 * 8 * nsplit * (128 * 4 + 8)
+    assert ws == (1824 * 4 + 32 * 8) * (128 * 4 + 8)
+    B = 2000
+    c = lib.attn_decode_chunk_len(B, 2, 4096)
+    assert lib.attn_decode_workspace_bytes(B, 8, 2, 128, 4096) == B * 8 * (4096 // c) * (128 * 4 + 8)
     assert lib.attn_decode_workspace_bytes(2, 3, 2, 128, 10) == 0

@@ -49,9 +49,14 @@ def test_decode_configured(name):
     (2, 16, 2, 128, 700, [700, 123]),        # G = 8
     (2, 6, 2, 128, 200, [200, 65]),          # G = 3 (one head per block)
     (3, 8, 2, 64, 513, [513, 64, 2]),        # D = 64
-    (1, 8, 1, 128, 40000, [40000]),          # long context, max chunk count
+    (1, 8, 1, 128, 40000, [40000]),          # long context, one sequence over every warp
+    (40, 8, 2, 128, 300, None),              # many short sequences per warp slice
 ])
 def test_decode_shapes(B, Hq, Hkv, D, max_len, lens):
+    if lens is None:  # lengths 0..max_len, including empty sequences
+        lens = torch.randint(0, max_len + 1, (B,), generator=torch.Generator().manual_seed(5))
+        lens[::7] = 0
+        lens = lens.tolist()
     q, kc, vc, sl = workloads.decode_inputs(B, Hq, Hkv, D, max_len, "explicit", seed=1,
                                             seqlens=lens)
     _check(q, kc, vc, sl, f"decode {B},{Hq},{Hkv},{D},{max_len},{lens}")
@@ -93,3 +98,13 @@ def test_decode_seqlen_above_max_len_is_clamped_and_flagged():
     o_ref, _ = oracle.decode(q, kc, vc, torch.tensor([96, 96], dtype=torch.int32),
                              1 / math.sqrt(128))
     check_out(o, o_ref, "bf16_pre", "clamped length")
+
+
+def test_decode_large_batch_chunked_path():
+    """Batches above 1024 use the chunked split kernel."""
+    B = 1100
+    lens = torch.randint(1, 97, (B,), generator=torch.Generator().manual_seed(6))
+    lens[::13] = 0
+    q, kc, vc, sl = workloads.decode_inputs(B, 8, 2, 128, 96, "explicit", seed=2,
+                                            seqlens=lens.tolist())
+    _check(q, kc, vc, sl, "decode B1100")
