@@ -64,15 +64,18 @@ def parse():
     p.add_argument("--prefill-batch", type=int, default=None)
     p.add_argument("--prefill-seq", type=int, default=None)
     p.add_argument("--decode-batch", type=int, default=None)
+    p.add_argument("--decode-len", type=int, default=None,
+                   help="every sequence this long (cache max_len too) instead of U[256, 4096]")
     args = p.parse_args()
     global PREFILL, DECODE
     if args.prefill_batch or args.prefill_seq:
         PREFILL = workloads.PrefillConfig("custom", args.prefill_batch or PREFILL.B, PREFILL.Hq,
                                           PREFILL.Hkv, args.prefill_seq or PREFILL.S, PREFILL.D,
                                           "bf16")
-    if args.decode_batch:
-        DECODE = workloads.DecodeConfig("custom", args.decode_batch, DECODE.Hq, DECODE.Hkv,
-                                        DECODE.D, DECODE.max_len, "uniform")
+    if args.decode_batch or args.decode_len:
+        DECODE = workloads.DecodeConfig("custom", args.decode_batch or DECODE.B, DECODE.Hq,
+                                        DECODE.Hkv, DECODE.D, args.decode_len or DECODE.max_len,
+                                        "full" if args.decode_len else "uniform")
     return args
 
 

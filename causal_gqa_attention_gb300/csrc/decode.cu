@@ -577,11 +577,14 @@ __global__ void __launch_bounds__(kWarps * 32)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Merge for the stream kernel: one block per (sequence, query head). Warp w combines pieces
-// w, w + 4, ... (in order), all its loads issued together; the four warp results are then
-// combined in warp order through shared memory, so the result does not depend on timing.
+// Merge for the stream kernel: one block of kStreamMergeWarps warps per (sequence, query head).
+// Warp w combines pieces w, w + kStreamMergeWarps, ... (in order, eight loads in flight at a
+// time); the warp results are then combined in warp order through shared memory, so the result
+// does not depend on timing.
+constexpr int kStreamMergeWarps = 16;
+
 template <bool OUT_F32, int D, int HG>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kStreamMergeWarps * 32)
     decode_stream_merge_kernel(const float *__restrict__ ws_o, const float2 *__restrict__ ws_ml,
                                const int *__restrict__ seqlens, void *__restrict__ o,
                                float *__restrict__ lse, int B, int Hq, int Hkv, int max_len,
@@ -589,8 +592,9 @@ __global__ void __launch_bounds__(128)
 {
     constexpr int DL = D / 32;
     constexpr int PW = 8;  // pieces per warp per round
-    __shared__ float s_acc[4][D];
-    __shared__ float s_m[4], s_l[4];
+    constexpr int MW = kStreamMergeWarps;
+    __shared__ float s_acc[MW][D];
+    __shared__ float s_m[MW], s_l[MW];
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int bh = blockIdx.x;
     const int b = bh / Hq, h = bh % Hq;
@@ -610,12 +614,12 @@ __global__ void __launch_bounds__(128)
     float M = -INFINITY, Ls = 0.f, acc[DL];
 #pragma unroll
     for (int e = 0; e < DL; ++e) acc[e] = 0.f;
-    for (int j0 = warp; j0 < n; j0 += 4 * PW) {
+    for (int j0 = warp; j0 < n; j0 += MW * PW) {
         float2 mlj[PW];
         float x[PW][DL];
 #pragma unroll
         for (int k = 0; k < PW; ++k) {
-            const int j = j0 + 4 * k;
+            const int j = j0 + MW * k;
             if (j < n) {
                 const size_t row = row0 + (size_t)j * HG;
                 mlj[k] = ws_ml[row];
@@ -653,13 +657,15 @@ __global__ void __launch_bounds__(128)
     }
     __syncthreads();
     if (warp == 0) {
-        float Mt = fmaxf(fmaxf(s_m[0], s_m[1]), fmaxf(s_m[2], s_m[3]));
+        float Mt = s_m[0];
+#pragma unroll
+        for (int w2 = 1; w2 < MW; ++w2) Mt = fmaxf(Mt, s_m[w2]);
         const float Mu = (Mt == -INFINITY) ? 0.f : Mt;
         float Lt = 0.f, r[DL];
 #pragma unroll
         for (int e = 0; e < DL; ++e) r[e] = 0.f;
-#pragma unroll
-        for (int w2 = 0; w2 < 4; ++w2) {
+#pragma unroll 4
+        for (int w2 = 0; w2 < MW; ++w2) {
             const float wgt = ex2(s_m[w2] - Mu);
             Lt = fmaf(wgt, s_l[w2], Lt);
 #pragma unroll
@@ -847,7 +853,7 @@ cudaError_t launch_stream_t(const DecodeArgs &a, bool out_f32, cudaStream_t st)
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.B * a.Hq);
-    cfg.blockDim = dim3(128);
+    cfg.blockDim = dim3(kStreamMergeWarps * 32);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
