@@ -110,6 +110,21 @@ int workspace_acquire(size_t need, cudaStream_t stream, bool may_grow, void **ou
     return ATTN_OK;
 }
 
+int sm_count(int *out)
+{
+    static int cached[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+        cached[dev] = n;
+    }
+    *out = cached[dev];
+    return ATTN_OK;
+}
+
 int check_prefill(const void *q, const void *k, const void *v, void *o, float *lse, int B,
                   int S, int Hq, int Hkv, int D, float scale, int in_t, int out_t)
 {
@@ -199,6 +214,26 @@ int attn_prefill_ex(const void *q, const void *k, const void *v, void *o, float 
     a.causal = causal ? 1 : 0;
     rc = status_ptr(&a.status);
     if (rc != ATTN_OK) return rc;
+    // Small grids (fewer row blocks x heads than SMs) split the keys of each row block over
+    // several blocks and merge; the partials use the library-owned scratch. If that scratch
+    // cannot grow now (stream capture), the unsplit kernel runs instead.
+    int sms = 0;
+    rc = sm_count(&sms);
+    if (rc != ATTN_OK) return rc;
+    int J = 0;
+    const size_t need = gqa::prefill_split_plan(B, S, Hq, causal ? 1 : 0, sms, &J);
+    if (J > 0) {
+        void *ws = nullptr;
+        rc = workspace_acquire(need, st, true, &ws);
+        if (rc == ATTN_OK) {
+            const size_t blocks = need / ((size_t)256 * 129 * sizeof(float));
+            a.J = J;
+            a.ws_o = static_cast<float *>(ws);
+            a.ws_lse = a.ws_o + blocks * 256 * 128;
+        } else if (rc != ATTN_ERR_WORKSPACE) {
+            return rc;
+        }
+    }
     return cuda_status(gqa::launch_prefill_tc(a, out_dtype == ATTN_F32, st));
 }
 

@@ -19,8 +19,15 @@ struct PrefillTcArgs {
     float scale_log2;  // scale * log2(e)
     int causal;
     unsigned *status;  // device status word
+    // key split for small grids (0 = none): blocks of at most J key tiles, partials in ws
+    int J = 0;
+    float *ws_o = nullptr;    // [blocks, 256, 128] fp32
+    float *ws_lse = nullptr;  // [blocks, 256] fp32
 };
 cudaError_t launch_prefill_tc(const PrefillTcArgs &a, bool out_f32, cudaStream_t stream);
+// Chooses the key split for a prefill shape on num_sms SMs: writes J (0 = no split) and returns
+// the workspace bytes it needs.
+size_t prefill_split_plan(int B, int S, int Hq, int causal, int num_sms, int *J);
 int prefill_tc_smem_bytes();
 
 // Prefill on CUDA cores in fp32 (fp32 q/k/v/o), head dim 64 or 128.

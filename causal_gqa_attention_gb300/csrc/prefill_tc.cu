@@ -79,10 +79,29 @@ enum : int {
     NUM_BARS = 18
 };
 
-__device__ __forceinline__ int last_key_tile(int causal, int q_first, int nkv)
+__host__ __device__ __forceinline__ int last_key_tile(int causal, int q_first, int nkv)
 {
     // causal: the tile whose rows start at q_first needs keys up to q_first + 127
-    return causal ? min((q_first + BM - 1) / BN, nkv - 1) : nkv - 1;
+    const int lim = (q_first + BM - 1) / BN;
+    return causal ? (lim < nkv - 1 ? lim : nkv - 1) : nkv - 1;
+}
+
+// Key tiles that the row block rb (rows 256 rb .. 256 rb + 255) visits.
+__host__ __device__ __forceinline__ int rb_key_tiles(int rb, int S, int causal)
+{
+    const int nkv = (S + BN - 1) / BN;
+    const int q0 = rb * 2 * BM;
+    const int l0 = last_key_tile(causal, q0, nkv);
+    const int l1 = (q0 + BM < S) ? last_key_tile(causal, q0 + BM, nkv) : -1;
+    return (l0 > l1 ? l0 : l1) + 1;
+}
+
+// Split mode: row block rb is cut into ceil(tiles / J) segments of at most J key tiles, each
+// one block. Blocks are numbered heaviest row block first: all segments of row block n_rb - 1
+// (segment-major, then batch x head), then n_rb - 2, ...
+__host__ __device__ __forceinline__ int rb_segments(int rb, int S, int causal, int J)
+{
+    return (rb_key_tiles(rb, S, causal) + J - 1) / J;
 }
 
 // 1 if either bf16 half of w has magnitude >= 2^16 (beyond the fp16 range) or is inf/NaN.
@@ -91,12 +110,17 @@ __device__ __forceinline__ uint32_t too_big_for_f16(uint32_t w)
     return (uint32_t)((w & 0x7FFF0000u) >= 0x47800000u) | (uint32_t)((w & 0x7FFFu) >= 0x4780u);
 }
 
-template <bool OUT_F32>
+// SPLIT = false: one block per (row block, head, batch), final O and LSE.
+// SPLIT = true: one block per (row block, key segment of J tiles, head, batch); it writes the
+// segment's normalised O (fp32) and its LSE (log2 units) to ws_o / ws_lse, and
+// prefill_split_merge_kernel combines the segments of each row.
+template <bool OUT_F32, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, void *__restrict__ out,
                       float *__restrict__ lse, int B, int S, int Hq, int Hkv, float scale_log2,
-                      int causal, unsigned *__restrict__ status)
+                      int causal, unsigned *__restrict__ status, int J, float *__restrict__ ws_o,
+                      float *__restrict__ ws_lse)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -109,9 +133,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- work item: heaviest row blocks first (causal), heads of one group adjacent
     const int n_rb = (S + 2 * BM - 1) / (2 * BM);
-    const int idx = blockIdx.x;
-    const int rb = n_rb - 1 - idx / (Hq * B);
-    const int hb = idx % (Hq * B);
+    int rb, hb, seg = 0;
+    if (!SPLIT) {
+        rb = n_rb - 1 - (int)blockIdx.x / (Hq * B);
+        hb = (int)blockIdx.x % (Hq * B);
+    } else {
+        int rem = (int)blockIdx.x;
+        for (rb = n_rb - 1; rb > 0; --rb) {
+            const int c = rb_segments(rb, S, causal, J) * Hq * B;
+            if (rem < c) break;
+            rem -= c;
+        }
+        seg = rem / (Hq * B);
+        hb = rem % (Hq * B);
+    }
     const int h = hb % Hq, b = hb / Hq;
     const int g = h / (Hq / Hkv);
     const int q0 = rb * 2 * BM;
@@ -121,6 +156,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     last_j[0] = last_key_tile(causal, q0, nkv);
     last_j[1] = (n_tiles == 2) ? last_key_tile(causal, q0 + BM, nkv) : -1;
     const int n_j = max(last_j[0], last_j[1]) + 1;
+    // key tiles [jb, je) of this block; tile t works on [jb, hi[t]] (empty when hi[t] < jb)
+    const int jb = SPLIT ? seg * J : 0;
+    const int je = SPLIT ? min(jb + J, n_j) : n_j;
+    const int nJ = je - jb;
+    int hi[2];
+    hi[0] = min(je - 1, last_j[0]);
+    hi[1] = min(je - 1, last_j[1]);
 
     if (threadIdx.x == 0) {
         mbar_init(&bar[B_Q], 1);
@@ -161,8 +203,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_3d(smem + kOffQ + t * kTile + x * kBox, &tq, &bar[B_Q], x * 64,
                                 q0 + t * BM, zq);
             int issued_k[2] = {0, 0}, issued_v[2] = {0, 0};
-            for (int j = 0; j < n_j; ++j) {
-                const int s = j & 1, use = j >> 1;
+            for (int jj = 0; jj < nJ; ++jj) {
+                const int j = jb + jj;
+                const int s = jj & 1, use = jj >> 1;
                 if (use > 0 && !mbar_wait(&bar[B_KEMPTY + s], (use - 1) & 1, abort_flag)) break;
                 mbar_arrive_expect_tx(&bar[B_KFULL + s], kTile);
                 for (int x = 0; x < 2; ++x)
@@ -195,35 +238,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t sK = smem_u32(smem + kOffK);
             const uint32_t sV = smem_u32(smem + kOffV);
             bool ok = mbar_wait(&bar[B_Q], 0, abort_flag);
-            for (int j = 0; ok && j <= n_j; ++j) {
-                const bool do_s = j < n_j;
-                const bool do_pv = j >= 1;
-                if (do_s && !mbar_wait(&bar[B_KFULL + (j & 1)], (j >> 1) & 1, abort_flag)) break;
+            for (int jj = 0; ok && jj <= nJ; ++jj) {
+                const int j = jb + jj;
+                const bool do_s = jj < nJ;
+                const bool do_pv = jj >= 1;
+                if (do_s && !mbar_wait(&bar[B_KFULL + (jj & 1)], (jj >> 1) & 1, abort_flag)) break;
                 if (do_pv &&
-                    !mbar_wait(&bar[B_VREADY + ((j - 1) & 1)], ((j - 1) >> 1) & 1, abort_flag))
+                    !mbar_wait(&bar[B_VREADY + ((jj - 1) & 1)], ((jj - 1) >> 1) & 1, abort_flag))
                     break;
                 tc_fence_after();
                 for (int t = 0; t < 2 && ok; ++t) {
-                    if (do_pv && j - 1 <= last_j[t]) {
-                        if (!mbar_wait(&bar[B_PFULL + t], (j - 1) & 1, abort_flag)) {
+                    if (do_pv && j - 1 <= hi[t]) {
+                        if (!mbar_wait(&bar[B_PFULL + t], (jj - 1) & 1, abort_flag)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t vbase = sV + ((j - 1) & 1) * kTile;
+                        const uint32_t vbase = sV + ((jj - 1) & 1) * kTile;
 #pragma unroll
                         for (int kk = 0; kk < BN / 16; ++kk) {
                             // B = V rows 16kk..16kk+15: MN-major, 64-col chunks 16 KB apart,
                             // 8-row groups 1 KB apart
                             const uint64_t bd = smem_desc_sw128(vbase + kk * 2048, kBox, 1024);
                             mma_ts(tmem + kColO + t * 128, tmem + kColS + t * 128 + kk * 8, bd,
-                                   idO, (j - 1 > 0 || kk > 0) ? 1u : 0u);
+                                   idO, (jj - 1 > 0 || kk > 0) ? 1u : 0u);
                         }
-                        if (j - 1 == last_j[t]) mma_commit(&bar[B_OFULL + t]);
+                        if (j - 1 == hi[t]) mma_commit(&bar[B_OFULL + t]);
                     }
-                    if (do_s && j <= last_j[t]) {
+                    if (do_s && j <= hi[t]) {
                         const uint32_t qbase = sQ + t * kTile;
-                        const uint32_t kbase = sK + (j & 1) * kTile;
+                        const uint32_t kbase = sK + (jj & 1) * kTile;
 #pragma unroll
                         for (int kk = 0; kk < HD / 16; ++kk) {
                             const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
@@ -235,8 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (!ok) break;
-                if (do_s) mma_commit(&bar[B_KEMPTY + (j & 1)]);
-                if (do_pv) mma_commit(&bar[B_VEMPTY + ((j - 1) & 1)]);
+                if (do_s) mma_commit(&bar[B_KEMPTY + (jj & 1)]);
+                if (do_pv) mma_commit(&bar[B_VEMPTY + ((jj - 1) & 1)]);
             }
             // drain: all issued tcgen05 work finishes before TMEM is released
             mma_commit(&bar[B_DRAIN]);
@@ -249,9 +293,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // is converted in place once it lands, then handed to the tensor core.
         const int ct = threadIdx.x - 64;
         uint32_t over = 0;
-        for (int j = 0; j < n_j; ++j) {
-            const int s = j & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(&bar[B_VFULL + s], (j >> 1) & 1, abort_flag)))
+        for (int jj = 0; jj < nJ; ++jj) {
+            const int s = jj & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&bar[B_VFULL + s], (jj >> 1) & 1, abort_flag)))
                 break;
             uint4 *tile = reinterpret_cast<uint4 *>(smem + kOffV + s * kTile);
 #pragma unroll 4
@@ -282,8 +326,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t < n_tiles) {
             float m_ref = -INFINITY, l = 0.f;
             bool ok = true;
-            for (int j = 0; j <= last_j[t]; ++j) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_SFULL + t], j & 1, abort_flag));
+            for (int j = jb; j <= hi[t]; ++j) {
+                const int jj = j - jb;
+                ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_SFULL + t], jj & 1, abort_flag));
                 if (!ok) break;
                 tc_fence_after();
                 uint32_t sv[128];  // raw fp32 bits of the row's scores
@@ -331,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 l = fmaf(l, alpha, (rsa.x + rsa.y) + (rsb.x + rsb.y));
                 tmem_st32(tS, &pk[0]);
                 tmem_st32(tS + 32, &pk[32]);
-                if (j > 0 && __any_sync(0xffffffffu, need)) {
+                if (jj > 0 && __any_sync(0xffffffffu, need)) {
                     uint32_t ov[128];
                     tmem_ld128(tO, ov);
                     const float2 a2 = make_float2(alpha, alpha);
@@ -351,9 +396,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&bar[B_PFULL + t]);
                 m_ref = m_new;
             }
-            if (ok)
+            const bool active = hi[t] >= jb;  // warp-uniform
+            if (ok && active)
                 ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_OFULL + t], 0, abort_flag));
-            if (ok) {
+            if (ok && SPLIT) {
+                // segment result: normalised O (fp32) and LSE in log2 units; an empty segment
+                // (this tile has no key tile in it) writes O = 0 and LSE = -inf
+                if (active) tc_fence_after();
+                const bool live = i < S;
+                const float inv = (active && l > 0.f) ? 1.f / l : 0.f;
+                const size_t prow = (size_t)blockIdx.x * (2 * BM) + t * BM + r;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t ov[32];
+                    if (active) tmem_ld32(tO + c * 32, ov);
+                    if (!live) continue;
+                    float4 *dst = reinterpret_cast<float4 *>(ws_o + prow * HD + c * 32);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        dst[e] = active ? make_float4(__uint_as_float(ov[4 * e]) * inv,
+                                                      __uint_as_float(ov[4 * e + 1]) * inv,
+                                                      __uint_as_float(ov[4 * e + 2]) * inv,
+                                                      __uint_as_float(ov[4 * e + 3]) * inv)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                if (live) ws_lse[prow] = (active && l > 0.f) ? m_ref + log2f(l) : -INFINITY;
+            } else if (ok) {
                 tc_fence_after();
                 const bool live = i < S;
                 const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -399,9 +467,73 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_dealloc(tmem, 512);
     }
     if (threadIdx.x == 0 && *abort_flag) atomicOr(status, 2u);
+    if (SPLIT) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Combine the key segments of each query row (split mode): one warp per row, four dims per
+// lane; segment weights 2^(lse_s - M), M = max_s lse_s, in segment order.
 template <bool OUT_F32>
+__global__ void __launch_bounds__(256)
+    prefill_split_merge_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_lse,
+                               void *__restrict__ out, float *__restrict__ lse, int B, int S,
+                               int Hq, int causal, int J)
+{
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const long long row = (long long)blockIdx.x * 8 + warp;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (row >= (long long)B * Hq * S) return;
+    const int i = (int)(row % S);
+    const int hb = (int)(row / S);  // b * Hq + h
+    const int n_rb = (S + 2 * BM - 1) / (2 * BM);
+    const int rb = i / (2 * BM), rloc = i % (2 * BM);
+    int first = 0;  // first block of row block rb
+    for (int r2 = n_rb - 1; r2 > rb; --r2) first += rb_segments(r2, S, causal, J) * Hq * B;
+    const int nseg = rb_segments(rb, S, causal, J);
+    // every load of the row in one round: segment LSEs and this lane's four dims of each O
+    float ls[8];
+    float4 x[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        ls[k] = -INFINITY;
+        x[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (k < nseg) {
+            const size_t item = (size_t)first + (size_t)k * Hq * B + hb;
+            ls[k] = ws_lse[item * (2 * BM) + rloc];
+            x[k] = *reinterpret_cast<const float4 *>(ws_o + (item * (2 * BM) + rloc) * HD +
+                                                     lane * 4);
+        }
+    }
+    float M = ls[0];
+#pragma unroll
+    for (int k = 1; k < 8; ++k) M = fmaxf(M, ls[k]);
+    const float Mu = (M == -INFINITY) ? 0.f : M;
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float w = ex2(ls[k] - Mu);  // 0 for absent segments
+        L += w;
+        acc.x = fmaf(w, x[k].x, acc.x);
+        acc.y = fmaf(w, x[k].y, acc.y);
+        acc.z = fmaf(w, x[k].z, acc.z);
+        acc.w = fmaf(w, x[k].w, acc.w);
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const size_t orow = (size_t)row;
+    if (OUT_F32) {
+        *reinterpret_cast<float4 *>(static_cast<float *>(out) + orow * HD + lane * 4) =
+            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    } else {
+        uint2 w2;
+        w2.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+        w2.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(out) + orow * HD + lane * 4) = w2;
+    }
+    if (lse != nullptr && lane == 0)
+        lse[orow] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+}
+
+template <bool OUT_F32, bool SPLIT>
 cudaError_t launch_t(const PrefillTcArgs &a, cudaStream_t st)
 {
     static bool attr_set[64] = {};  // the attribute is set once per device
@@ -409,16 +541,34 @@ cudaError_t launch_t(const PrefillTcArgs &a, cudaStream_t st)
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 64 || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(prefill_tc_kernel<OUT_F32>,
+        e = cudaFuncSetAttribute(prefill_tc_kernel<OUT_F32, SPLIT>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (e != cudaSuccess) return e;
         if (dev < 64) attr_set[dev] = true;
     }
     const int n_rb = (a.S + 2 * BM - 1) / (2 * BM);
-    const long long blocks = (long long)n_rb * a.Hq * a.B;
-    prefill_tc_kernel<OUT_F32><<<(unsigned)blocks, kThreads, kSmem, st>>>(
-        a.tq, a.tk, a.tv, a.o, a.lse, a.B, a.S, a.Hq, a.Hkv, a.scale_log2, a.causal, a.status);
-    return cudaGetLastError();
+    long long blocks = (long long)n_rb * a.Hq * a.B;
+    if (SPLIT) {
+        blocks = 0;
+        for (int rb = 0; rb < n_rb; ++rb) blocks += (long long)rb_segments(rb, a.S, a.causal, a.J) * a.Hq * a.B;
+    }
+    prefill_tc_kernel<OUT_F32, SPLIT><<<(unsigned)blocks, kThreads, kSmem, st>>>(
+        a.tq, a.tk, a.tv, a.o, a.lse, a.B, a.S, a.Hq, a.Hkv, a.scale_log2, a.causal, a.status,
+        a.J, a.ws_o, a.ws_lse);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || !SPLIT) return e;
+    const long long rows = (long long)a.B * a.Hq * a.S;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((rows + 7) / 8));
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prefill_split_merge_kernel<OUT_F32>, (const float *)a.ws_o,
+                              (const float *)a.ws_lse, a.o, a.lse, a.B, a.S, a.Hq, a.causal, a.J);
 }
 
 }  // namespace
@@ -427,7 +577,38 @@ int prefill_tc_smem_bytes() { return (int)kSmem; }
 
 cudaError_t launch_prefill_tc(const PrefillTcArgs &a, bool out_f32, cudaStream_t st)
 {
-    return out_f32 ? launch_t<true>(a, st) : launch_t<false>(a, st);
+    if (a.J > 0) return out_f32 ? launch_t<true, true>(a, st) : launch_t<false, true>(a, st);
+    return out_f32 ? launch_t<true, false>(a, st) : launch_t<false, false>(a, st);
+}
+
+size_t prefill_split_plan(int B, int S, int Hq, int causal, int num_sms, int *J_out)
+{
+    // Split the key range only when the plain grid leaves SMs idle: pick the longest segment
+    // (fewest blocks) whose grid still fits in one wave; at most 8 segments per row block.
+    *J_out = 0;
+    const int n_rb = (S + 2 * BM - 1) / (2 * BM);
+    const long long plain = (long long)n_rb * Hq * B;
+    if (plain >= num_sms) return 0;
+    const int nmax = rb_key_tiles(n_rb - 1, S, causal) > rb_key_tiles(0, S, causal)
+                         ? rb_key_tiles(n_rb - 1, S, causal)
+                         : rb_key_tiles(0, S, causal);
+    int best = 0;
+    for (int J = nmax - 1; J >= 2; --J) {
+        long long blocks = 0;
+        bool fits = true;
+        for (int rb = 0; rb < n_rb; ++rb) {
+            const int ns = rb_segments(rb, S, causal, J);
+            if (ns > 8) fits = false;
+            blocks += (long long)ns * Hq * B;
+        }
+        if (!fits || blocks > num_sms) break;
+        best = J;
+    }
+    if (best == 0) return 0;
+    *J_out = best;
+    long long blocks = 0;
+    for (int rb = 0; rb < n_rb; ++rb) blocks += (long long)rb_segments(rb, S, causal, best) * Hq * B;
+    return (size_t)blocks * (2 * BM) * (HD + 1) * sizeof(float);
 }
 
 }  // namespace gqa

@@ -72,6 +72,10 @@ typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype;
  *   scale multiplies the scores before the softmax (usually 1/sqrt(D)).
  *   causal != 0: query i sees keys 0..i.
  * Requires Hq % Hkv == 0, D == 128, 16-byte aligned pointers.
+ * When the shape has fewer (256-row block, head) tiles than the GPU has SMs, the key range of
+ * each row block is split over several thread blocks and a second kernel merges their results
+ * by log-sum-exp weights; the partial results use the library-owned scratch buffer (grown with
+ * cudaMalloc on first use, outside stream capture; during capture the unsplit kernel runs).
  * Computes on tcgen05 tensor cores with fp32 accumulation and fp32 softmax state: Q K^T from
  * the bf16 inputs; P V with P rounded to fp16 and V converted bf16 -> fp16 on chip (exact for
  * 2^-14 <= |v| <= 65280; larger |v| saturate and set ATTN_DEV_FP16_RANGE in the status word).
