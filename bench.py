@@ -79,6 +79,39 @@ def parse():
     return args
 
 
+def recorded_traffic():
+    """DRAM traffic per launch recorded from ncu in profiles/, valid only while the kernel source
+    it was measured on is unchanged (sha256 prefix of the kernel file + ptx.cuh)."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "dram_traffic_prefill_b8s8192_decode_b32.md")
+    csrc = os.path.join(ROOT, "causal_gqa_attention_gb300", "csrc")
+    out = {"prefill_tc_kernel": None, "decode_stream_kernel": None}
+    if not os.path.exists(path):
+        return out
+    text = open(path).read()
+
+    def sha(*names):
+        h = hashlib.sha256()
+        for n in names:
+            h.update(open(os.path.join(csrc, n), "rb").read())
+        return h.hexdigest()[:16]
+
+    cur = {"prefill_tc_kernel": sha("prefill_tc.cu", "ptx.cuh"),
+           "decode_stream_kernel": sha("decode.cu", "ptx.cuh")}
+    tag = {"prefill_tc_kernel": "prefill_tc.cu+ptx.cuh", "decode_stream_kernel": "decode.cu+ptx.cuh"}
+    for kname in out:
+        rec_sha, rec_bytes = None, None
+        for line in text.splitlines():
+            if line.startswith(f"source-sha {tag[kname]}:"):
+                rec_sha = line.split(":", 1)[1].strip()
+            if line.startswith(f"traffic-bytes {kname}:"):
+                rec_bytes = int(line.split(":", 1)[1].strip())
+        if rec_sha == cur[kname] and rec_bytes:
+            out[kname] = rec_bytes
+    return out
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -348,19 +381,19 @@ def main():
     b2b = None
     if args.only != "prefill":
         sets = []
-        for k in range(DECODE_SETS):
-            tq, tkc, tvc, tsl = workloads.config_decode_inputs(DECODE, seed=100 + k, nan_fill=False)
+        for si in range(DECODE_SETS):
+            tq, tkc, tvc, tsl = workloads.config_decode_inputs(DECODE, seed=100 + si, nan_fill=False)
             nb = workloads.decode_bytes(tsl.tolist(), DECODE.Hq, DECODE.Hkv, DECODE.D)
             sets.append((tq.to(dev), tkc.to(dev), tvc.to(dev), tsl.to(dev), nb))
         outs = [torch.empty_like(x[0]) for x in sets]
-        for k in range(DECODE_SETS):  # warm (first-use set-up happens outside capture)
-            cga.decode(sets[k][0], sets[k][1], sets[k][2], sets[k][3], out=outs[k])
+        for si in range(DECODE_SETS):  # warm (first-use set-up happens outside capture)
+            cga.decode(sets[si][0], sets[si][1], sets[si][2], sets[si][3], out=outs[si])
         torch.cuda.synchronize()
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             for c in range(DECODE_CALLS):
-                k = c % DECODE_SETS
-                cga.decode(sets[k][0], sets[k][1], sets[k][2], sets[k][3], out=outs[k])
+                si = c % DECODE_SETS
+                cga.decode(sets[si][0], sets[si][1], sets[si][2], sets[si][3], out=outs[si])
         graph.replay()
         torch.cuda.synchronize()
         g_ms = []
@@ -438,6 +471,7 @@ def main():
         return
     if rank == 0:
         peak_t = pk["bf16_tflops"]
+        traffic = recorded_traffic()
         line = {
             "metric": METRIC,
             "value": tflops * world,
@@ -459,9 +493,14 @@ def main():
                        "back_to_back": b2b,
                        "roofline": {"bound": "hbm", "achieved": dec_gbs,
                                     "peak": pk["hbm_gbs"], "unit": "GB/s",
-                                    "frac": dec_gbs / pk["hbm_gbs"], "traffic": None}},
+                                    "frac": dec_gbs / pk["hbm_gbs"],
+                                    "traffic": traffic["decode_stream_kernel"]
+                                    if args.decode_batch is None and args.decode_len is None
+                                    else None}},
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak_t,
-                         "unit": "TFLOP/s", "frac": tflops / peak_t, "traffic": None,
+                         "unit": "TFLOP/s", "frac": tflops / peak_t,
+                         "traffic": traffic["prefill_tc_kernel"]
+                         if args.prefill_batch is None and args.prefill_seq is None else None,
                          "kernel": "prefill_tc_kernel", "peak_source": pk["source"]},
             "e2e": e2e,
             "cpu_baseline": cpu,
