@@ -54,9 +54,11 @@ constexpr int kThreads = 384;  // 12 warps
 constexpr uint32_t kBox = 16384;          // one 128-row x 64-col bf16 box (128-byte rows)
 constexpr uint32_t kTile = 2 * kBox;      // 128 x 128 bf16
 constexpr uint32_t kOffQ = 0;             // 2 tiles
-constexpr uint32_t kOffK = 2 * kTile;     // 2 stages
-constexpr uint32_t kOffV = 4 * kTile;     // 2 stages
-constexpr uint32_t kOffBar = 6 * kTile;
+constexpr int KST = 2;                    // K ring stages
+constexpr int VST = 3;                    // V ring stages (V also waits for its fp16 conversion)
+constexpr uint32_t kOffK = 2 * kTile;
+constexpr uint32_t kOffV = kOffK + KST * kTile;
+constexpr uint32_t kOffBar = kOffV + VST * kTile;
 constexpr uint32_t kSmem = kOffBar + 256 + 1024;  // + barriers, + alignment slack
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
 
@@ -67,17 +69,19 @@ constexpr uint32_t kColO = 256;  // + 128 t
 // barrier indices
 enum : int {
     B_Q = 0,
-    B_KFULL = 1,   // 2
-    B_KEMPTY = 3,  // 2
-    B_VFULL = 5,   // 2
-    B_VEMPTY = 7,  // 2
-    B_SFULL = 9,   // 2 (per tile)
-    B_PFULL = 11,  // 2 (per tile)
-    B_OFULL = 13,  // 2 (per tile)
-    B_DRAIN = 15,
-    B_VREADY = 16,  // 2: V stage converted to fp16
-    NUM_BARS = 18
+    B_KFULL = 1,                // KST
+    B_KEMPTY = B_KFULL + KST,   // KST
+    B_VFULL = B_KEMPTY + KST,   // VST
+    B_VEMPTY = B_VFULL + VST,   // VST
+    B_VREADY = B_VEMPTY + VST,  // VST: V stage converted to fp16
+    B_SFULL = B_VREADY + VST,   // 2 (per tile)
+    B_PFULL = B_SFULL + 2,      // 2 (per tile)
+    B_OFULL = B_PFULL + 2,      // 2 (per tile)
+    B_DRAIN = B_OFULL + 2,
+    NUM_BARS = B_DRAIN + 1
 };
+static_assert(NUM_BARS * 8 + 8 <= 256, "barrier area");
+static_assert(kSmem <= 232448, "shared memory per block");
 
 __host__ __device__ __forceinline__ int last_key_tile(int causal, int q_first, int nkv)
 {
@@ -166,18 +170,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(&bar[B_Q], 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < KST; ++s) {
             mbar_init(&bar[B_KFULL + s], 1);
             mbar_init(&bar[B_KEMPTY + s], 1);
+        }
+        for (int s = 0; s < VST; ++s) {
             mbar_init(&bar[B_VFULL + s], 1);
             mbar_init(&bar[B_VEMPTY + s], 1);
-            mbar_init(&bar[B_SFULL + s], 1);
-            mbar_init(&bar[B_PFULL + s], BM);
-            mbar_init(&bar[B_OFULL + s], 1);
+            mbar_init(&bar[B_VREADY + s], 64);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&bar[B_SFULL + t], 1);
+            mbar_init(&bar[B_PFULL + t], BM);
+            mbar_init(&bar[B_OFULL + t], 1);
         }
         mbar_init(&bar[B_DRAIN], 1);
-        mbar_init(&bar[B_VREADY], 64);
-        mbar_init(&bar[B_VREADY + 1], 64);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -202,31 +209,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int x = 0; x < 2; ++x)
                     tma_load_3d(smem + kOffQ + t * kTile + x * kBox, &tq, &bar[B_Q], x * 64,
                                 q0 + t * BM, zq);
-            int issued_k[2] = {0, 0}, issued_v[2] = {0, 0};
+            int issued_k[KST] = {}, issued_v[VST] = {};
             for (int jj = 0; jj < nJ; ++jj) {
                 const int j = jb + jj;
-                const int s = jj & 1, use = jj >> 1;
-                if (use > 0 && !mbar_wait(&bar[B_KEMPTY + s], (use - 1) & 1, abort_flag)) break;
-                mbar_arrive_expect_tx(&bar[B_KFULL + s], kTile);
+                const int sk = jj % KST, uk = jj / KST;
+                if (uk > 0 && !mbar_wait(&bar[B_KEMPTY + sk], (uk - 1) & 1, abort_flag)) break;
+                mbar_arrive_expect_tx(&bar[B_KFULL + sk], kTile);
                 for (int x = 0; x < 2; ++x)
-                    tma_load_3d(smem + kOffK + s * kTile + x * kBox, &tk, &bar[B_KFULL + s],
+                    tma_load_3d(smem + kOffK + sk * kTile + x * kBox, &tk, &bar[B_KFULL + sk],
                                 x * 64, j * BN, zk);
-                issued_k[s] = use + 1;
-                if (use > 0 && !mbar_wait(&bar[B_VEMPTY + s], (use - 1) & 1, abort_flag)) break;
-                mbar_arrive_expect_tx(&bar[B_VFULL + s], kTile);
+                issued_k[sk] = uk + 1;
+                const int sv = jj % VST, uv = jj / VST;
+                if (uv > 0 && !mbar_wait(&bar[B_VEMPTY + sv], (uv - 1) & 1, abort_flag)) break;
+                mbar_arrive_expect_tx(&bar[B_VFULL + sv], kTile);
                 for (int x = 0; x < 2; ++x)
-                    tma_load_3d(smem + kOffV + s * kTile + x * kBox, &tv, &bar[B_VFULL + s],
+                    tma_load_3d(smem + kOffV + sv * kTile + x * kBox, &tv, &bar[B_VFULL + sv],
                                 x * 64, j * BN, zk);
-                issued_v[s] = use + 1;
+                issued_v[sv] = uv + 1;
             }
             if (*abort_flag) {
                 // let every copy this block started land before the block exits
                 volatile int never = 0;
                 mbar_wait(&bar[B_Q], 0, &never);
-                for (int s = 0; s < 2; ++s) {
+                for (int s = 0; s < KST; ++s)
                     if (issued_k[s]) mbar_wait(&bar[B_KFULL + s], (issued_k[s] - 1) & 1, &never);
+                for (int s = 0; s < VST; ++s)
                     if (issued_v[s]) mbar_wait(&bar[B_VFULL + s], (issued_v[s] - 1) & 1, &never);
-                }
             }
         }
     } else if (warp == 1) {
@@ -242,9 +250,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int j = jb + jj;
                 const bool do_s = jj < nJ;
                 const bool do_pv = jj >= 1;
-                if (do_s && !mbar_wait(&bar[B_KFULL + (jj & 1)], (jj >> 1) & 1, abort_flag)) break;
+                if (do_s && !mbar_wait(&bar[B_KFULL + jj % KST], (jj / KST) & 1, abort_flag)) break;
                 if (do_pv &&
-                    !mbar_wait(&bar[B_VREADY + ((jj - 1) & 1)], ((jj - 1) >> 1) & 1, abort_flag))
+                    !mbar_wait(&bar[B_VREADY + (jj - 1) % VST], ((jj - 1) / VST) & 1, abort_flag))
                     break;
                 tc_fence_after();
                 for (int t = 0; t < 2 && ok; ++t) {
@@ -254,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t vbase = sV + ((jj - 1) & 1) * kTile;
+                        const uint32_t vbase = sV + ((jj - 1) % VST) * kTile;
 #pragma unroll
                         for (int kk = 0; kk < BN / 16; ++kk) {
                             // B = V rows 16kk..16kk+15: MN-major, 64-col chunks 16 KB apart,
@@ -267,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (do_s && j <= hi[t]) {
                         const uint32_t qbase = sQ + t * kTile;
-                        const uint32_t kbase = sK + (jj & 1) * kTile;
+                        const uint32_t kbase = sK + (jj % KST) * kTile;
 #pragma unroll
                         for (int kk = 0; kk < HD / 16; ++kk) {
                             const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
@@ -279,8 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (!ok) break;
-                if (do_s) mma_commit(&bar[B_KEMPTY + (jj & 1)]);
-                if (do_pv) mma_commit(&bar[B_VEMPTY + ((jj - 1) & 1)]);
+                if (do_s) mma_commit(&bar[B_KEMPTY + jj % KST]);
+                if (do_pv) mma_commit(&bar[B_VEMPTY + (jj - 1) % VST]);
             }
             // drain: all issued tcgen05 work finishes before TMEM is released
             mma_commit(&bar[B_DRAIN]);
@@ -294,8 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ct = threadIdx.x - 64;
         uint32_t over = 0;
         for (int jj = 0; jj < nJ; ++jj) {
-            const int s = jj & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(&bar[B_VFULL + s], (jj >> 1) & 1, abort_flag)))
+            const int s = jj % VST;
+            if (!__all_sync(0xffffffffu, mbar_wait(&bar[B_VFULL + s], (jj / VST) & 1, abort_flag)))
                 break;
             uint4 *tile = reinterpret_cast<uint4 *>(smem + kOffV + s * kTile);
 #pragma unroll 4
