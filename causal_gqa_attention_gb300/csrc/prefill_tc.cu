@@ -368,22 +368,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float2 sc2 = make_float2(scale_log2, scale_log2);
                 const float2 nm2 = make_float2(-mu, -mu);
                 float2 rsa = make_float2(0.f, 0.f), rsb = rsa;
-                uint32_t pk[64];
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                    const float2 x = ffma2(make_float2(__uint_as_float(sv[2 * c]),
-                                                       __uint_as_float(sv[2 * c + 1])),
-                                           sc2, nm2);
-                    const float2 p = make_float2(ex2(x.x), ex2(x.y));
-                    if (c & 1)
-                        rsb = fadd2(rsb, p);
-                    else
-                        rsa = fadd2(rsa, p);
-                    pk[c] = pack_f16x2(p.x, p.y);
+                for (int half = 0; half < 2; ++half) {  // 32 packed columns at a time
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        const int e = half * 64 + 2 * c;
+                        const float2 x = ffma2(make_float2(__uint_as_float(sv[e]),
+                                                           __uint_as_float(sv[e + 1])),
+                                               sc2, nm2);
+                        const float2 p = make_float2(ex2(x.x), ex2(x.y));
+                        if (c & 1)
+                            rsb = fadd2(rsb, p);
+                        else
+                            rsa = fadd2(rsa, p);
+                        pk[c] = pack_f16x2(p.x, p.y);
+                    }
+                    tmem_st32(tS + half * 32, pk);
                 }
                 l = fmaf(l, alpha, (rsa.x + rsa.y) + (rsb.x + rsb.y));
-                tmem_st32(tS, &pk[0]);
-                tmem_st32(tS + 32, &pk[32]);
                 if (jj > 0 && __any_sync(0xffffffffu, need)) {
                     uint32_t ov[128];
                     tmem_ld128(tO, ov);

@@ -53,6 +53,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// Same, but the thread may be suspended (up to `ns` nanoseconds) until the phase completes
+// instead of returning at once: waiting warps then take no issue slots from working ones.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+                 : "memory");
+    return ok != 0;
+}
+
 // Upper bound on one wait, in SM clock cycles (about 2 s at 2 GHz). A correct pipeline waits
 // microseconds; running out means a miscounted barrier, and the block gives up instead of
 // hanging the GPU.
@@ -65,7 +79,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
         if (*abort) return false;
         if (clock64() - t0 > kWaitLimitCycles) {
             *abort = 1;

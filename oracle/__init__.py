@@ -57,6 +57,10 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_decode.argtypes = [_dp, _dp, _dp, _i32p, _dp, _dp, ctypes.c_int, ctypes.c_int,
                                   ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
                                   ctypes.c_int]
+    lib.oracle_chunk.restype = ctypes.c_int
+    lib.oracle_chunk.argtypes = [_dp, _dp, _dp, _i32p, _dp, _dp, ctypes.c_int, ctypes.c_int,
+                                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                 ctypes.c_double, ctypes.c_int, ctypes.c_int]
     lib.oracle_row_partial.restype = None
     lib.oracle_row_partial.argtypes = [_dp, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_double,
                                        _dp, _dp, _dp]
@@ -142,6 +146,28 @@ def decode(q, kcache, vcache, seqlens, scale: float, nthreads: int = 0, lib=None
                            B, Hq, Hkv, D, max_len, float(scale), nthreads)
     if rc != 0:
         raise ValueError("oracle_decode rejected its arguments")
+    return o, lse
+
+
+def chunk(q, kcache, vcache, seqlens, scale: float, causal: bool = True, nthreads: int = 0,
+          lib=None):
+    """Sq new queries per sequence against a cache: q [B,Hq,Sq,D], caches [B,Hkv,max_len,D],
+    seqlens [B]; query i of sequence b is at position seqlens[b] - Sq + i.
+    Returns (o [B,Hq,Sq,D], lse [B,Hq,Sq]) in float64."""
+    lib = lib or load()
+    q, kc, vc = _f64(q), _f64(kcache), _f64(vcache)
+    if hasattr(seqlens, "detach"):
+        seqlens = seqlens.detach().to("cpu").numpy()
+    sl = np.ascontiguousarray(np.asarray(seqlens, dtype=np.int32))
+    B, Hq, Sq, D = q.shape
+    Hkv, max_len = kc.shape[1], kc.shape[2]
+    assert kc.shape == (B, Hkv, max_len, D) and vc.shape == kc.shape and sl.shape == (B,)
+    o = np.empty((B, Hq, Sq, D))
+    lse = np.empty((B, Hq, Sq))
+    rc = lib.oracle_chunk(_p(q), _p(kc), _p(vc), sl.ctypes.data_as(_i32p), _p(o), _p(lse), B, Sq,
+                          Hq, Hkv, D, max_len, float(scale), int(bool(causal)), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_chunk rejected its arguments")
     return o, lse
 
 

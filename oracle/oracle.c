@@ -176,6 +176,49 @@ int oracle_decode(const double *q, const double *kc, const double *vc, const int
     return bad;
 }
 
+/* A chunk of Sq new queries against a KV cache: query i of sequence b sits at position
+ * p = L_b - Sq + i (the chunk is the last Sq tokens, already written to the cache), sees keys
+ * j < L_b, and with the causal mask only j <= p. Queries at p < 0 see nothing (O = 0, LSE = -inf).
+ * With Sq = L_b this is prefill; with Sq = 1 it is decode.
+ *   q [B, Hq, Sq, D], k/v cache [B, Hkv, max_len, D], seqlens [B], o [B, Hq, Sq, D], lse [B, Hq, Sq]
+ * ("Hand-written Triton decoder", section 1.4: speculative decoding and beam search reuse the
+ * same attention with several new tokens; "Attention three-op fusion", section 4.3: the causal
+ * mask as -infinity.) */
+int oracle_chunk(const double *q, const double *kc, const double *vc, const int32_t *seqlens,
+                 double *o, double *lse, int B, int Sq, int Hq, int Hkv, int D, int max_len,
+                 double scale, int causal, int nthreads)
+{
+    if (B < 0 || Sq < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || max_len < 0 || Hq % Hkv != 0) return 1;
+    for (int b = 0; b < B; ++b)
+        if (seqlens[b] < 0 || seqlens[b] > max_len) return 1;
+    const int G = Hq / Hkv;
+    set_threads(nthreads);
+    int bad = 0;
+#pragma omp parallel reduction(| : bad)
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+        unsigned char *vis = (unsigned char *)malloc((size_t)(max_len > 0 ? max_len : 1));
+        if (!s || !vis) bad = 1;
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t r = 0; r < (int64_t)B * Hq * Sq; ++r) {
+            if (!s || !vis) continue;
+            const int i = (int)(r % Sq);
+            const int h = (int)((r / Sq) % Hq);
+            const int b = (int)(r / ((int64_t)Sq * Hq));
+            const int g = h / G;
+            const int L = seqlens[b];
+            const long long p = (long long)L - Sq + i;
+            for (int j = 0; j < L; ++j) vis[j] = causal ? ((long long)j <= p) : 1;
+            const double *kb = kc + ((int64_t)b * Hkv + g) * max_len * D;
+            const double *vb = vc + ((int64_t)b * Hkv + g) * max_len * D;
+            attend_row(q + r * D, kb, vb, D, L, vis, D, scale, s, o + r * D, lse + r);
+        }
+        free(s);
+        free(vis);
+    }
+    return bad;
+}
+
 /* ---- the method: online softmax over key blocks, and the merge of block partials ---- */
 
 /* Partial state of one query row over n keys (one block): m = max score, l = sum of

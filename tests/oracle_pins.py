@@ -279,8 +279,38 @@ def pin_hard_max_limit(lib):
     _close(lse[0, 0], np.full(S, k[0, 0, j, 0]), 0.0, "hard max lse")
 
 
+def pin_chunk_reduces_to_prefill_and_decode(lib):
+    """A chunk of all L_b tokens is causal prefill of the sequence; a chunk of one token is
+    decode; a chunk of the last c tokens equals the last c rows of prefill."""
+    rng = _rng(11)
+    B, Hq, Hkv, S, D = 2, 4, 2, 21, 5
+    q = rng.standard_normal((B, Hq, S, D)); k = rng.standard_normal((B, Hkv, S, D))
+    v = rng.standard_normal((B, Hkv, S, D))
+    o, lse = oracle.prefill(q, k, v, True, 0.45, lib=lib)
+    max_len = S + 3
+    kc = np.full((B, Hkv, max_len, D), np.nan); vc = np.full((B, Hkv, max_len, D), np.nan)
+    kc[:, :, :S] = k; vc[:, :, :S] = v
+    oc, lsec = oracle.chunk(q, kc, vc, [S, S], 0.45, True, lib=lib)
+    _close(oc, o, 1e-13, "chunk = prefill O")
+    _close(lsec, lse, 1e-13, "chunk = prefill lse")
+    for c in (1, 4):
+        oc, lsec = oracle.chunk(q[:, :, S - c:], kc, vc, [S, S], 0.45, True, lib=lib)
+        _close(oc, o[:, :, S - c:], 1e-13, f"chunk of {c} = last prefill rows")
+    od, lsed = oracle.decode(q[:, :, -1], kc, vc, [S, S], 0.45, lib=lib)
+    oc, lsec = oracle.chunk(q[:, :, -1:], kc, vc, [S, S], 0.45, True, lib=lib)
+    _close(oc[:, :, 0], od, 1e-13, "chunk of 1 = decode")
+    # non-causal chunk: every query sees all L_b keys, as decode does
+    oc, _ = oracle.chunk(q[:, :, :3], kc, vc, [S, 7], 0.45, False, lib=lib)
+    for i in range(3):
+        od, _ = oracle.decode(q[:, :, i], kc, vc, [S, 7], 0.45, lib=lib)
+        _close(oc[:, :, i], od, 1e-13, "non-causal chunk = decode per query")
+    # a query before the start of the sequence sees nothing
+    oc, lsec = oracle.chunk(q[:, :, :4], kc, vc, [2, S], 0.45, True, lib=lib)
+    assert np.all(oc[0, :, :2] == 0) and np.all(np.isneginf(lsec[0, :, :2]))
+
+
 ALL_PINS = [pin_rows_of_p_sum_to_one, pin_constant_keys_give_prefix_means,
             pin_single_key_returns_v, pin_two_keys_closed_form, pin_shift_invariance,
             pin_gqa_equals_repeated_heads, pin_brute_force_tiny, pin_merge_is_order_free,
             pin_online_equals_two_pass, pin_decode_is_last_prefill_row, pin_empty_decode_row,
-            pin_hard_max_limit]
+            pin_hard_max_limit, pin_chunk_reduces_to_prefill_and_decode]

@@ -33,12 +33,16 @@ MUTANTS = [
     ("lse_missing_max", "*lse = m + log(l);\n}\n\nstatic", "*lse = log(l);\n}\n\nstatic"),
     ("row_max_skipped", "for (int j = 0; j < n_keys; ++j) if (s[j] > m) m = s[j];",
      "m = 0.0;"),
-    ("decode_drops_newest", "attend_row(q + r * D, kb, vb, D, L, vis,",
-     "attend_row(q + r * D, kb, vb, D, (L > 0 ? L - 1 : 0), vis,"),
+    ("decode_drops_newest", "for (int j = 0; j < L; ++j) vis[j] = 1;",
+     "for (int j = 0; j < L; ++j) vis[j] = (j < L - 1);"),
     ("merge_weight_dropped", "L += l[i] * w;", "L += l[i];"),
     ("online_no_rescale", "l *= c;\n        for (int d = 0; d < D; ++d) acc[d] *= c;",
      "for (int d = 0; d < D; ++d) acc[d] *= c;"),
     ("partial_no_max", "double e = exp(s[j] - m);", "double e = exp(s[j]);"),
+    ("chunk_offset_dropped", "const long long p = (long long)L - Sq + i;",
+     "const long long p = (long long)i;"),
+    ("chunk_strict_causal", "vis[j] = causal ? ((long long)j <= p) : 1;",
+     "vis[j] = causal ? ((long long)j < p) : 1;"),
 ]
 
 
