@@ -22,7 +22,8 @@ from ._lib import (ATTN_BF16, ATTN_DEV_FP16_RANGE, ATTN_DEV_SEQLEN_CLAMPED, ATTN
                    ATTN_ERR_WORKSPACE, ATTN_F32, ATTN_OK, AttnError)
 
 __all__ = [
-    "attn_prefill", "attn_prefill_ex", "attn_decode", "attn_decode_ex", "attn_decode_noalloc",
+    "attn_prefill", "attn_prefill_ex", "attn_chunk", "attn_decode", "attn_decode_ex",
+    "attn_decode_noalloc", "chunk",
     "attn_decode_workspace_bytes", "attn_decode_chunk_len", "attn_reserve_workspace",
     "attn_device_status", "attn_status_string", "attn_version", "prefill", "decode",
     "device_status", "AttnError", "ATTN_OK", "ATTN_ERR_INVALID", "ATTN_ERR_UNSUPPORTED",
@@ -46,6 +47,12 @@ def attn_prefill_ex(q, k, v, o, lse, B, S, Hq, Hkv, D, scale, causal, in_dtype, 
                     stream):
     return _lib.load().attn_prefill_ex(q, k, v, o, lse, B, S, Hq, Hkv, D, scale, causal,
                                        in_dtype, out_dtype, stream)
+
+
+def attn_chunk(q, kcache, vcache, seqlens, o, lse, B, Sq, Hq, Hkv, D, max_len, scale, causal,
+               out_dtype, stream):
+    return _lib.load().attn_chunk(q, kcache, vcache, seqlens, o, lse, B, Sq, Hq, Hkv, D, max_len,
+                                  scale, causal, out_dtype, stream)
 
 
 def attn_decode(q, kcache, vcache, seqlens, o, B, Hq, Hkv, D, max_len, scale, stream):
@@ -151,6 +158,41 @@ def prefill(q, k, v, causal: bool = True, scale: float | None = None, out_dtype=
                              float(scale), int(bool(causal)), in_t, out_t,
                              _stream_handle(q.device))
     _lib.check("attn_prefill_ex", rc)
+    return (out, lse) if return_lse else out
+
+
+def chunk(q, kcache, vcache, seqlens, causal: bool = True, scale: float | None = None,
+          out_dtype=None, return_lse: bool = False, out=None, lse=None):
+    """Sq new queries per sequence against a bf16 KV cache: q [B,Hq,Sq,D] bf16 (the last Sq
+    tokens of each sequence, already in the cache), caches [B,Hkv,max_len,D] bf16, seqlens [B]
+    int32 on the device. Query i of sequence b sits at position seqlens[b] - Sq + i.
+    Returns o [B,Hq,Sq,D] (bf16 by default), or (o, lse [B,Hq,Sq])."""
+    torch = _torch()
+    B, Hq, Sq, D = q.shape
+    Hkv, max_len = kcache.shape[1], kcache.shape[2]
+    if kcache.shape != (B, Hkv, max_len, D) or vcache.shape != kcache.shape:
+        raise ValueError("cache shapes do not match q")
+    _check_cuda("q", q, torch.bfloat16)
+    _check_cuda("kcache", kcache, torch.bfloat16)
+    _check_cuda("vcache", vcache, torch.bfloat16)
+    _check_cuda("seqlens", seqlens, torch.int32)
+    if seqlens.shape != (B,):
+        raise ValueError("seqlens must be [B]")
+    out_dtype = out_dtype or torch.bfloat16
+    if out is None:
+        out = torch.empty((B, Hq, Sq, D), dtype=out_dtype, device=q.device)
+    else:
+        _check_cuda("out", out, out_dtype)
+    if return_lse and lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    out_t = ATTN_BF16 if out_dtype == torch.bfloat16 else ATTN_F32
+    with torch.cuda.device(q.device):
+        rc = attn_chunk(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(seqlens), _ptr(out), _ptr(lse),
+                        B, Sq, Hq, Hkv, D, max_len, float(scale), int(bool(causal)), out_t,
+                        _stream_handle(q.device))
+    _lib.check("attn_chunk", rc)
     return (out, lse) if return_lse else out
 
 

@@ -237,6 +237,39 @@ int attn_prefill_ex(const void *q, const void *k, const void *v, void *o, float 
     return cuda_status(gqa::launch_prefill_tc(a, out_dtype == ATTN_F32, st));
 }
 
+int attn_chunk(const void *q, const void *kcache, const void *vcache, const int *seqlens,
+               void *o, float *lse, int B, int Sq, int Hq, int Hkv, int D, int max_len,
+               float scale, int causal, int out_dtype, void *stream)
+{
+    if (!seqlens) return ATTN_ERR_INVALID;
+    if (max_len <= 0) return ATTN_ERR_INVALID;
+    int rc = check_prefill(q, kcache, vcache, o, lse, B, Sq, Hq, Hkv, D, scale, ATTN_BF16,
+                           out_dtype);
+    if (rc != ATTN_OK) return rc;
+    if (!aligned4(seqlens)) return ATTN_ERR_ALIGN;
+    if ((long long)B * Hkv * max_len > (1LL << 40)) return ATTN_ERR_UNSUPPORTED;
+    PrefillTcArgs a;
+    std::memset(&a, 0, sizeof(a));
+    if (!encode_bf16_rows(&a.tq, q, (long long)B * Hq, Sq) ||
+        !encode_bf16_rows(&a.tk, kcache, (long long)B * Hkv, max_len) ||
+        !encode_bf16_rows(&a.tv, vcache, (long long)B * Hkv, max_len))
+        return ATTN_ERR_CUDA;
+    a.o = o;
+    a.lse = lse;
+    a.B = B;
+    a.S = Sq;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.causal = causal ? 1 : 0;
+    a.kv_lens = seqlens;
+    a.max_kv = max_len;
+    rc = status_ptr(&a.status);
+    if (rc != ATTN_OK) return rc;
+    return cuda_status(gqa::launch_prefill_tc(a, out_dtype == ATTN_F32,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
 int attn_prefill(const void *q, const void *k, const void *v, void *o, float *lse, int B, int S,
                  int Hq, int Hkv, int D, float scale, int causal, void *stream)
 {

@@ -19,6 +19,10 @@ struct PrefillTcArgs {
     float scale_log2;  // scale * log2(e)
     int causal;
     unsigned *status;  // device status word
+    // chunk against a cache: k/v maps view [B*Hkv, max_kv rows]; kv_lens[b] keys per sequence
+    // (device); the S queries are the last S of them. nullptr: plain prefill (L = S).
+    const int *kv_lens = nullptr;
+    int max_kv = 0;
     // key split for small grids (0 = none): blocks of at most J key tiles, partials in ws
     int J = 0;
     float *ws_o = nullptr;    // [blocks, 256, 128] fp32

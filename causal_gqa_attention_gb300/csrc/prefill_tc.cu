@@ -85,9 +85,13 @@ static_assert(kSmem <= 232448, "shared memory per block");
 
 __host__ __device__ __forceinline__ int last_key_tile(int causal, int q_first, int nkv)
 {
-    // causal: the tile whose rows start at q_first needs keys up to q_first + 127
-    const int lim = (q_first + BM - 1) / BN;
-    return causal ? (lim < nkv - 1 ? lim : nkv - 1) : nkv - 1;
+    // causal: the tile whose rows start at key position q_first needs keys up to q_first + 127
+    // (-1: no key at all)
+    if (!causal) return nkv - 1;
+    const int last = q_first + BM - 1;
+    if (last < 0) return -1;
+    const int lim = last / BN;
+    return lim < nkv - 1 ? lim : nkv - 1;
 }
 
 // Key tiles that the row block rb (rows 256 rb .. 256 rb + 255) visits.
@@ -124,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tv, void *__restrict__ out,
                       float *__restrict__ lse, int B, int S, int Hq, int Hkv, float scale_log2,
                       int causal, unsigned *__restrict__ status, int J, float *__restrict__ ws_o,
-                      float *__restrict__ ws_lse)
+                      float *__restrict__ ws_lse, const int *__restrict__ kv_lens, int max_kv)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -154,12 +158,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = hb % Hq, b = hb / Hq;
     const int g = h / (Hq / Hkv);
     const int q0 = rb * 2 * BM;
-    const int nkv = (S + BN - 1) / BN;
+    // Keys: L of them. Plain prefill: L = S. Chunk against a cache (kv_lens given): the S
+    // queries are the last S of the L_b cached tokens, so query row i sits at key position
+    // i + off, off = L_b - S.
+    int L = S;
+    if (kv_lens != nullptr) {
+        L = kv_lens[b];
+        if (L < 0 || L > max_kv) {
+            if (threadIdx.x == 0 && rb == n_rb - 1 && h == 0) atomicOr(status, 1u);
+            L = L < 0 ? 0 : max_kv;
+        }
+    }
+    const int off = L - S;
+    const int nkv = (L + BN - 1) / BN;
     const int n_tiles = (q0 + BM < S) ? 2 : 1;
     int last_j[2];
-    last_j[0] = last_key_tile(causal, q0, nkv);
-    last_j[1] = (n_tiles == 2) ? last_key_tile(causal, q0 + BM, nkv) : -1;
-    const int n_j = max(last_j[0], last_j[1]) + 1;
+    last_j[0] = last_key_tile(causal, q0 + off, nkv);
+    last_j[1] = (n_tiles == 2) ? last_key_tile(causal, q0 + BM + off, nkv) : -1;
+    const int n_j = max(last_j[0], last_j[1]) + 1;  // 0: no key at all (O = 0, LSE = -inf)
     // key tiles [jb, je) of this block; tile t works on [jb, hi[t]] (empty when hi[t] < jb)
     const int jb = SPLIT ? seg * J : 0;
     const int je = SPLIT ? min(jb + J, n_j) : n_j;
@@ -306,9 +322,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!__all_sync(0xffffffffu, mbar_wait(&bar[B_VFULL + s], (jj / VST) & 1, abort_flag)))
                 break;
             uint4 *tile = reinterpret_cast<uint4 *>(smem + kOffV + s * kTile);
+            // rows at or past L (a cache's stale rows may hold anything) become 0: p is 0
+            // there, but 0 * NaN would not be
+            const int rows_ok = L - (jb + jj) * BN;
 #pragma unroll 4
             for (int c = ct; c < (int)(kTile / 16); c += 64) {
                 uint4 w = tile[c];
+                if (((c & 1023) >> 3) >= rows_ok) w = make_uint4(0, 0, 0, 0);
                 // |bf16| >= 2^16 (magnitude bits >= 0x4780) does not fit fp16; inf, NaN too
                 over |= too_big_for_f16(w.x) | too_big_for_f16(w.y) | too_big_for_f16(w.z) |
                         too_big_for_f16(w.w);
@@ -342,8 +362,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t sv[128];  // raw fp32 bits of the row's scores
                 tmem_ld128(tS, sv);
                 const int k0 = j * BN;
-                if (k0 + BN > S || (causal && k0 + BN - 1 > i)) {
-                    const int lim = causal ? min(i + 1, S) : S;  // keys < lim are visible
+                if (k0 + BN > L || (causal && k0 + BN - 1 > i + off)) {
+                    const int lim = causal ? min(i + off + 1, L) : L;  // keys < lim are visible
 #pragma unroll
                     for (int c = 0; c < 128; ++c)
                         if (k0 + c >= lim) sv[c] = __float_as_uint(-INFINITY);
@@ -433,14 +453,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (live) ws_lse[prow] = (active && l > 0.f) ? m_ref + log2f(l) : -INFINITY;
             } else if (ok) {
-                tc_fence_after();
+                // an inactive tile (its rows see no key) writes O = 0 and LSE = -inf
+                if (active) tc_fence_after();
                 const bool live = i < S;
-                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const float inv = (active && l > 0.f) ? 1.f / l : 0.f;
                 const size_t orow = ((size_t)b * Hq + h) * S + (live ? i : 0);
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
                     uint32_t ov[32];
-                    tmem_ld32(tO + c * 32, ov);
+                    if (active)
+                        tmem_ld32(tO + c * 32, ov);
+                    else
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) ov[e] = 0u;
                     if (!live) continue;
                     if (OUT_F32) {
                         float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(out) +
@@ -466,7 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (live && lse != nullptr)
-                    lse[orow] = l > 0.f ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
+                    lse[orow] = (active && l > 0.f) ? (m_ref + log2f(l)) * 0.69314718055994531f
+                                                    : -INFINITY;
             }
         }
     }
@@ -565,7 +591,7 @@ cudaError_t launch_t(const PrefillTcArgs &a, cudaStream_t st)
     }
     prefill_tc_kernel<OUT_F32, SPLIT><<<(unsigned)blocks, kThreads, kSmem, st>>>(
         a.tq, a.tk, a.tv, a.o, a.lse, a.B, a.S, a.Hq, a.Hkv, a.scale_log2, a.causal, a.status,
-        a.J, a.ws_o, a.ws_lse);
+        a.J, a.ws_o, a.ws_lse, a.kv_lens, a.kv_lens ? a.max_kv : a.S);
     e = cudaGetLastError();
     if (e != cudaSuccess || !SPLIT) return e;
     const long long rows = (long long)a.B * a.Hq * a.S;

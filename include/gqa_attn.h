@@ -97,6 +97,28 @@ int attn_prefill_ex(const void *q, const void *k, const void *v, void *o, float 
                     int out_dtype, void *stream);
 
 /*
+ * attn_chunk -- a chunk of Sq new query tokens per sequence against a bf16 KV cache (chunked
+ * prefill, verification of speculative tokens). The chunk is the last Sq tokens of each
+ * sequence and is already in the cache, so query i of sequence b sits at position
+ * p = seqlens[b] - Sq + i; it sees cache rows j < seqlens[b], and with causal != 0 only j <= p.
+ * A query with p < 0 sees nothing: o = 0, lse = -inf.
+ *   q        [B, Hq, Sq, D] bf16
+ *   kcache   [B, Hkv, max_len, D] bf16, vcache likewise; rows >= seqlens[b] are masked (their
+ *            contents never reach the result, NaN included)
+ *   seqlens  [B] int32, device memory; values outside [0, max_len] are clamped and flagged
+ *            (ATTN_DEV_SEQLEN_CLAMPED)
+ *   o        [B, Hq, Sq, D], bf16 or fp32 by out_dtype; lse [B, Hq, Sq] fp32 or NULL
+ * Requires Hq % Hkv == 0, D == 128. Same tensor-core kernel as attn_prefill (with
+ * seqlens[b] = Sq = S, max_len = S it computes exactly attn_prefill's result).
+ * Sources: "Hand-written Triton decoder" (m.nlpx.cn/news/28229) section 1.4 (speculative
+ * decoding and beam search reuse the attention kernels with several new tokens);
+ * "Attention three-op fusion" (xdnf.cn/news/349386) section 4.3 (causal and padding masks).
+ */
+int attn_chunk(const void *q, const void *kcache, const void *vcache, const int *seqlens,
+               void *o, float *lse, int B, int Sq, int Hq, int Hkv, int D, int max_len,
+               float scale, int causal, int out_dtype, void *stream);
+
+/*
  * attn_decode -- one query token per sequence against a bf16 KV cache.
  *   q        [B, Hq, D] bf16
  *   kcache   [B, Hkv, max_len, D] bf16, vcache likewise; rows >= seqlens[b] are never read
