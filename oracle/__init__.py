@@ -61,6 +61,10 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_chunk.argtypes = [_dp, _dp, _dp, _i32p, _dp, _dp, ctypes.c_int, ctypes.c_int,
                                  ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                  ctypes.c_double, ctypes.c_int, ctypes.c_int]
+    lib.oracle_prefill_varlen.restype = ctypes.c_int
+    lib.oracle_prefill_varlen.argtypes = [_dp, _dp, _dp, _i32p, _dp, _dp, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_double, ctypes.c_int, ctypes.c_int]
     lib.oracle_row_partial.restype = None
     lib.oracle_row_partial.argtypes = [_dp, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_double,
                                        _dp, _dp, _dp]
@@ -168,6 +172,26 @@ def chunk(q, kcache, vcache, seqlens, scale: float, causal: bool = True, nthread
                           Hq, Hkv, D, max_len, float(scale), int(bool(causal)), nthreads)
     if rc != 0:
         raise ValueError("oracle_chunk rejected its arguments")
+    return o, lse
+
+
+def prefill_varlen(q, k, v, seqlens, causal: bool, scale: float, nthreads: int = 0, lib=None):
+    """Padded batch: q [B,Hq,S,D], k/v [B,Hkv,S,D], sequence b valid in its first seqlens[b]
+    tokens; padding rows give O = 0, LSE = -inf. Returns (o, lse) in float64."""
+    lib = lib or load()
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    if hasattr(seqlens, "detach"):
+        seqlens = seqlens.detach().to("cpu").numpy()
+    sl = np.ascontiguousarray(np.asarray(seqlens, dtype=np.int32))
+    B, Hq, S, D = q.shape
+    Hkv = k.shape[1]
+    assert k.shape == (B, Hkv, S, D) and v.shape == k.shape and sl.shape == (B,)
+    o = np.empty((B, Hq, S, D))
+    lse = np.empty((B, Hq, S))
+    rc = lib.oracle_prefill_varlen(_p(q), _p(k), _p(v), sl.ctypes.data_as(_i32p), _p(o), _p(lse),
+                                   B, S, Hq, Hkv, D, float(scale), int(bool(causal)), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_prefill_varlen rejected its arguments")
     return o, lse
 
 

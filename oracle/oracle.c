@@ -219,6 +219,44 @@ int oracle_chunk(const double *q, const double *kc, const double *vc, const int3
     return bad;
 }
 
+/* Batched prefill of sequences padded to S tokens: sequence b holds seqlens[b] valid tokens at
+ * positions 0 .. seqlens[b]-1. Row i < L_b sees keys j < L_b (and j <= i when causal); padding
+ * rows i >= L_b see nothing (O = 0, LSE = -inf). Layouts as oracle_prefill.
+ * ("Attention three-op fusion", section 4.3: padding positions get score -infinity.) */
+int oracle_prefill_varlen(const double *q, const double *k, const double *v, const int32_t *seqlens,
+                          double *o, double *lse, int B, int S, int Hq, int Hkv, int D,
+                          double scale, int causal, int nthreads)
+{
+    if (B < 0 || S < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv != 0) return 1;
+    for (int b = 0; b < B; ++b)
+        if (seqlens[b] < 0 || seqlens[b] > S) return 1;
+    const int G = Hq / Hkv;
+    set_threads(nthreads);
+    int bad = 0;
+#pragma omp parallel reduction(| : bad)
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(S > 0 ? S : 1));
+        unsigned char *vis = (unsigned char *)malloc((size_t)(S > 0 ? S : 1));
+        if (!s || !vis) bad = 1;
+#pragma omp for schedule(dynamic, 8)
+        for (int64_t r = 0; r < (int64_t)B * Hq * S; ++r) {
+            if (!s || !vis) continue;
+            const int i = (int)(r % S);
+            const int h = (int)((r / S) % Hq);
+            const int b = (int)(r / ((int64_t)S * Hq));
+            const int g = h / G;
+            const int L = seqlens[b];
+            for (int j = 0; j < L; ++j) vis[j] = (i < L) && (causal ? (j <= i) : 1);
+            const double *kb = k + ((int64_t)b * Hkv + g) * S * D;
+            const double *vb = v + ((int64_t)b * Hkv + g) * S * D;
+            attend_row(q + r * D, kb, vb, D, L, vis, D, scale, s, o + r * D, lse + r);
+        }
+        free(s);
+        free(vis);
+    }
+    return bad;
+}
+
 /* ---- the method: online softmax over key blocks, and the merge of block partials ---- */
 
 /* Partial state of one query row over n keys (one block): m = max score, l = sum of

@@ -309,8 +309,31 @@ def pin_chunk_reduces_to_prefill_and_decode(lib):
     assert np.all(oc[0, :, :2] == 0) and np.all(np.isneginf(lsec[0, :, :2]))
 
 
+def pin_varlen_is_prefill_of_each_sequence(lib):
+    """Each sequence of a padded batch equals prefill of its own valid tokens; padding rows are
+    O = 0, LSE = -inf; full lengths give plain prefill."""
+    rng = _rng(12)
+    B, Hq, Hkv, S, D = 3, 4, 2, 17, 6
+    q = rng.standard_normal((B, Hq, S, D)); k = rng.standard_normal((B, Hkv, S, D))
+    v = rng.standard_normal((B, Hkv, S, D))
+    lens = [17, 9, 0]
+    for causal in (True, False):
+        o, lse = oracle.prefill_varlen(q, k, v, lens, causal, 0.4, lib=lib)
+        for b, L in enumerate(lens):
+            if L:
+                ob, lb = oracle.prefill(q[b:b + 1, :, :L], k[b:b + 1, :, :L], v[b:b + 1, :, :L],
+                                        causal, 0.4, lib=lib)
+                _close(o[b:b + 1, :, :L], ob, 1e-13, f"varlen seq {b}")
+                _close(lse[b:b + 1, :, :L], lb, 1e-13, f"varlen lse {b}")
+            assert np.all(o[b, :, L:] == 0) and np.all(np.isneginf(lse[b, :, L:])), "padding rows"
+        of, lf = oracle.prefill_varlen(q, k, v, [S, S, S], causal, 0.4, lib=lib)
+        op, lp = oracle.prefill(q, k, v, causal, 0.4, lib=lib)
+        assert np.array_equal(of, op) and np.array_equal(lf, lp)
+
+
 ALL_PINS = [pin_rows_of_p_sum_to_one, pin_constant_keys_give_prefix_means,
             pin_single_key_returns_v, pin_two_keys_closed_form, pin_shift_invariance,
             pin_gqa_equals_repeated_heads, pin_brute_force_tiny, pin_merge_is_order_free,
             pin_online_equals_two_pass, pin_decode_is_last_prefill_row, pin_empty_decode_row,
-            pin_hard_max_limit, pin_chunk_reduces_to_prefill_and_decode]
+            pin_hard_max_limit, pin_chunk_reduces_to_prefill_and_decode,
+            pin_varlen_is_prefill_of_each_sequence]

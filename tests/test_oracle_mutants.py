@@ -41,6 +41,8 @@ MUTANTS = [
     ("partial_no_max", "double e = exp(s[j] - m);", "double e = exp(s[j]);"),
     ("chunk_offset_dropped", "const long long p = (long long)L - Sq + i;",
      "const long long p = (long long)i;"),
+    ("varlen_padding_rows_live", "vis[j] = (i < L) && (causal ? (j <= i) : 1);",
+     "vis[j] = (causal ? (j <= i) : 1);"),
     ("chunk_strict_causal", "vis[j] = causal ? ((long long)j <= p) : 1;",
      "vis[j] = causal ? ((long long)j < p) : 1;"),
 ]
