@@ -22,7 +22,7 @@ from ._lib import (ATTN_BF16, ATTN_DEV_FP16_RANGE, ATTN_DEV_SEQLEN_CLAMPED, ATTN
                    ATTN_ERR_WORKSPACE, ATTN_F32, ATTN_OK, AttnError)
 
 __all__ = [
-    "attn_prefill", "attn_prefill_ex", "attn_chunk", "attn_decode", "attn_decode_ex",
+    "attn_prefill", "attn_prefill_ex", "attn_prefill_varlen", "prefill_varlen", "attn_chunk", "attn_decode", "attn_decode_ex",
     "attn_decode_noalloc", "chunk",
     "attn_decode_workspace_bytes", "attn_decode_chunk_len", "attn_reserve_workspace",
     "attn_device_status", "attn_status_string", "attn_version", "prefill", "decode",
@@ -47,6 +47,12 @@ def attn_prefill_ex(q, k, v, o, lse, B, S, Hq, Hkv, D, scale, causal, in_dtype, 
                     stream):
     return _lib.load().attn_prefill_ex(q, k, v, o, lse, B, S, Hq, Hkv, D, scale, causal,
                                        in_dtype, out_dtype, stream)
+
+
+def attn_prefill_varlen(q, k, v, seqlens, o, lse, B, S, Hq, Hkv, D, scale, causal, out_dtype,
+                        stream):
+    return _lib.load().attn_prefill_varlen(q, k, v, seqlens, o, lse, B, S, Hq, Hkv, D, scale,
+                                           causal, out_dtype, stream)
 
 
 def attn_chunk(q, kcache, vcache, seqlens, o, lse, B, Sq, Hq, Hkv, D, max_len, scale, causal,
@@ -193,6 +199,38 @@ def chunk(q, kcache, vcache, seqlens, causal: bool = True, scale: float | None =
                         B, Sq, Hq, Hkv, D, max_len, float(scale), int(bool(causal)), out_t,
                         _stream_handle(q.device))
     _lib.check("attn_chunk", rc)
+    return (out, lse) if return_lse else out
+
+
+def prefill_varlen(q, k, v, seqlens, causal: bool = True, scale: float | None = None,
+                   out_dtype=None, return_lse: bool = False, out=None, lse=None):
+    """Padded batch: q [B,Hq,S,D], k/v [B,Hkv,S,D] bf16, sequence b valid in its first seqlens[b]
+    tokens (seqlens int32 on the device). Padding rows give o = 0 (lse = -inf)."""
+    torch = _torch()
+    B, Hq, S, D = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (B, Hkv, S, D) or v.shape != k.shape:
+        raise ValueError("k/v shapes do not match q")
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _check_cuda(n, t, torch.bfloat16)
+    _check_cuda("seqlens", seqlens, torch.int32)
+    if seqlens.shape != (B,):
+        raise ValueError("seqlens must be [B]")
+    out_dtype = out_dtype or torch.bfloat16
+    if out is None:
+        out = torch.empty((B, Hq, S, D), dtype=out_dtype, device=q.device)
+    else:
+        _check_cuda("out", out, out_dtype)
+    if return_lse and lse is None:
+        lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    out_t = ATTN_BF16 if out_dtype == torch.bfloat16 else ATTN_F32
+    with torch.cuda.device(q.device):
+        rc = attn_prefill_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(seqlens), _ptr(out), _ptr(lse), B,
+                                 S, Hq, Hkv, D, float(scale), int(bool(causal)), out_t,
+                                 _stream_handle(q.device))
+    _lib.check("attn_prefill_varlen", rc)
     return (out, lse) if return_lse else out
 
 

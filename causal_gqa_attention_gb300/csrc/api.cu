@@ -237,9 +237,34 @@ int attn_prefill_ex(const void *q, const void *k, const void *v, void *o, float 
     return cuda_status(gqa::launch_prefill_tc(a, out_dtype == ATTN_F32, st));
 }
 
+namespace {
+int chunk_or_varlen(const void *q, const void *kc, const void *vc, const int *seqlens, void *o,
+                    float *lse, int B, int Sq, int Hq, int Hkv, int D, int max_len, float scale,
+                    int causal, int out_dtype, int front, void *stream);
+}  // namespace
+
+int attn_prefill_varlen(const void *q, const void *k, const void *v, const int *seqlens, void *o,
+                        float *lse, int B, int S, int Hq, int Hkv, int D, float scale, int causal,
+                        int out_dtype, void *stream)
+{
+    return chunk_or_varlen(q, k, v, seqlens, o, lse, B, S, Hq, Hkv, D, S, scale, causal,
+                           out_dtype, 1, stream);
+}
+
 int attn_chunk(const void *q, const void *kcache, const void *vcache, const int *seqlens,
                void *o, float *lse, int B, int Sq, int Hq, int Hkv, int D, int max_len,
                float scale, int causal, int out_dtype, void *stream)
+{
+    return chunk_or_varlen(q, kcache, vcache, seqlens, o, lse, B, Sq, Hq, Hkv, D, max_len, scale,
+                           causal, out_dtype, 0, stream);
+}
+
+}  // extern "C"
+
+namespace {
+int chunk_or_varlen(const void *q, const void *kcache, const void *vcache, const int *seqlens,
+                    void *o, float *lse, int B, int Sq, int Hq, int Hkv, int D, int max_len,
+                    float scale, int causal, int out_dtype, int front, void *stream)
 {
     if (!seqlens) return ATTN_ERR_INVALID;
     if (max_len <= 0) return ATTN_ERR_INVALID;
@@ -264,11 +289,15 @@ int attn_chunk(const void *q, const void *kcache, const void *vcache, const int 
     a.causal = causal ? 1 : 0;
     a.kv_lens = seqlens;
     a.max_kv = max_len;
+    a.front = front;
     rc = status_ptr(&a.status);
     if (rc != ATTN_OK) return rc;
     return cuda_status(gqa::launch_prefill_tc(a, out_dtype == ATTN_F32,
                                               static_cast<cudaStream_t>(stream)));
 }
+}  // namespace
+
+extern "C" {
 
 int attn_prefill(const void *q, const void *k, const void *v, void *o, float *lse, int B, int S,
                  int Hq, int Hkv, int D, float scale, int causal, void *stream)

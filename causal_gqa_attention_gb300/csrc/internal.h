@@ -23,6 +23,9 @@ struct PrefillTcArgs {
     // (device); the S queries are the last S of them. nullptr: plain prefill (L = S).
     const int *kv_lens = nullptr;
     int max_kv = 0;
+    // with kv_lens: 0 = the queries are the last S tokens (cache chunk); 1 = the queries are
+    // tokens 0..S-1 of a padded batch, kv_lens[b] of them valid (rows past it are padding)
+    int front = 0;
     // key split for small grids (0 = none): blocks of at most J key tiles, partials in ws
     int J = 0;
     float *ws_o = nullptr;    // [blocks, 256, 128] fp32

@@ -128,7 +128,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tv, void *__restrict__ out,
                       float *__restrict__ lse, int B, int S, int Hq, int Hkv, float scale_log2,
                       int causal, unsigned *__restrict__ status, int J, float *__restrict__ ws_o,
-                      float *__restrict__ ws_lse, const int *__restrict__ kv_lens, int max_kv)
+                      float *__restrict__ ws_lse, const int *__restrict__ kv_lens, int max_kv,
+                      int front)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -169,12 +170,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             L = L < 0 ? 0 : max_kv;
         }
     }
-    const int off = L - S;
+    // front != 0 (padded batch): the L valid queries are rows 0..L-1 (off = 0) and rows >= L
+    // are padding that sees no key
+    const int off = front ? 0 : L - S;
     const int nkv = (L + BN - 1) / BN;
     const int n_tiles = (q0 + BM < S) ? 2 : 1;
     int last_j[2];
-    last_j[0] = last_key_tile(causal, q0 + off, nkv);
-    last_j[1] = (n_tiles == 2) ? last_key_tile(causal, q0 + BM + off, nkv) : -1;
+    last_j[0] = (front && q0 >= L) ? -1 : last_key_tile(causal, q0 + off, nkv);
+    last_j[1] = (n_tiles == 2 && !(front && q0 + BM >= L))
+                    ? last_key_tile(causal, q0 + BM + off, nkv)
+                    : -1;
     const int n_j = max(last_j[0], last_j[1]) + 1;  // 0: no key at all (O = 0, LSE = -inf)
     // key tiles [jb, je) of this block; tile t works on [jb, hi[t]] (empty when hi[t] < jb)
     const int jb = SPLIT ? seg * J : 0;
@@ -362,8 +367,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t sv[128];  // raw fp32 bits of the row's scores
                 tmem_ld128(tS, sv);
                 const int k0 = j * BN;
-                if (k0 + BN > L || (causal && k0 + BN - 1 > i + off)) {
-                    const int lim = causal ? min(i + off + 1, L) : L;  // keys < lim are visible
+                const bool dead = front && i >= L;  // padding row
+                if (k0 + BN > L || (causal && k0 + BN - 1 > i + off) || dead) {
+                    const int lim = dead ? 0 : (causal ? min(i + off + 1, L) : L);  // keys < lim
 #pragma unroll
                     for (int c = 0; c < 128; ++c)
                         if (k0 + c >= lim) sv[c] = __float_as_uint(-INFINITY);
@@ -591,7 +597,7 @@ cudaError_t launch_t(const PrefillTcArgs &a, cudaStream_t st)
     }
     prefill_tc_kernel<OUT_F32, SPLIT><<<(unsigned)blocks, kThreads, kSmem, st>>>(
         a.tq, a.tk, a.tv, a.o, a.lse, a.B, a.S, a.Hq, a.Hkv, a.scale_log2, a.causal, a.status,
-        a.J, a.ws_o, a.ws_lse, a.kv_lens, a.kv_lens ? a.max_kv : a.S);
+        a.J, a.ws_o, a.ws_lse, a.kv_lens, a.kv_lens ? a.max_kv : a.S, a.front);
     e = cudaGetLastError();
     if (e != cudaSuccess || !SPLIT) return e;
     const long long rows = (long long)a.B * a.Hq * a.S;

@@ -119,6 +119,21 @@ int attn_chunk(const void *q, const void *kcache, const void *vcache, const int 
                float scale, int causal, int out_dtype, void *stream);
 
 /*
+ * attn_prefill_varlen -- batched prefill of sequences of different lengths, padded to S tokens.
+ * Sequence b holds seqlens[b] valid tokens at positions 0 .. seqlens[b]-1 of q, k, v; keys at
+ * or past seqlens[b] are masked (their contents never reach the result); padding rows
+ * (i >= seqlens[b]) get o = 0 and lse = -inf.
+ *   q [B, Hq, S, D] bf16, k/v [B, Hkv, S, D] bf16, seqlens [B] int32 (device, clamped to
+ *   [0, S] and flagged with ATTN_DEV_SEQLEN_CLAMPED), o [B, Hq, S, D] bf16 or fp32 by
+ *   out_dtype, lse [B, Hq, S] fp32 or NULL. Requires Hq % Hkv == 0, D == 128.
+ * Source: "Attention three-op fusion" (xdnf.cn/news/349386) section 4.3 (padding mask: positions
+ * at or past the sequence length get score -infinity) and section 6.1 (dynamic shapes).
+ */
+int attn_prefill_varlen(const void *q, const void *k, const void *v, const int *seqlens, void *o,
+                        float *lse, int B, int S, int Hq, int Hkv, int D, float scale, int causal,
+                        int out_dtype, void *stream);
+
+/*
  * attn_decode -- one query token per sequence against a bf16 KV cache.
  *   q        [B, Hq, D] bf16
  *   kcache   [B, Hkv, max_len, D] bf16, vcache likewise; rows >= seqlens[b] are never read
