@@ -57,6 +57,8 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-extras", action="store_true",
+                   help="skip the extra timings (cache chunk, padded varlen prefill)")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle sample")
     p.add_argument("--only", default="all", choices=["all", "prefill", "decode"],
@@ -295,6 +297,57 @@ def config_block():
     }
 
 
+# --------------------------------------------------------------------------- extra paths
+
+
+def _time(fn, flush, stream, reps):
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        flush()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts)
+
+
+def time_extras(cga, dev, stream, flush, steps):
+    """Timings of the wider paths on representative shapes (one call each, clean L2)."""
+    out = {}
+    # chunked prefill: 8 sequences, 512 new tokens each against caches of 4096..8192 tokens
+    B, Hq, Hkv, D, Sq, max_len = 8, 8, 2, 128, 512, 8192
+    g = torch.Generator().manual_seed(0)
+    lens = torch.randint(4096, max_len + 1, (B,), generator=g, dtype=torch.int32)
+    q = torch.randn((B, Hq, Sq, D), generator=g).to(torch.bfloat16).to(dev)
+    kc = torch.randn((B, Hkv, max_len, D), generator=g).to(torch.bfloat16).to(dev)
+    vc = torch.randn((B, Hkv, max_len, D), generator=g).to(torch.bfloat16).to(dev)
+    dl = lens.to(dev)
+    o = torch.empty_like(q)
+    ms = _time(lambda: cga.chunk(q, kc, vc, dl, out=o), flush, stream, max(3, steps // 2))
+    pairs = sum(int(L) * Sq - Sq * (Sq - 1) // 2 for L in lens.tolist())
+    fl = 4 * Hq * D * pairs
+    out["chunk_b8_sq512_kv4096to8192"] = {"ms": ms, "value": fl / (ms * 1e-3) / 1e12,
+                                          "unit": "TFLOP/s", "flops": fl}
+    del q, kc, vc, o
+    # padded variable-length prefill: 8 sequences of 1024..8192 tokens padded to 8192
+    S = 8192
+    lens = torch.randint(1024, S + 1, (B,), generator=g, dtype=torch.int32)
+    q, k, v = [t.to(dev) for t in workloads.prefill_inputs(B, Hq, Hkv, S, D, "bf16", seed=3)]
+    dl = lens.to(dev)
+    o = torch.empty_like(q)
+    ms = _time(lambda: cga.prefill_varlen(q, k, v, dl, out=o), flush, stream, max(3, steps // 2))
+    fl = sum(workloads.prefill_flops(1, Hq, int(L), D, True) for L in lens.tolist())
+    out["varlen_b8_s1024to8192_padded8192"] = {"ms": ms, "value": fl / (ms * 1e-3) / 1e12,
+                                               "unit": "TFLOP/s", "flops": fl}
+    return out
+
+
 # --------------------------------------------------------------------------- our kernels
 
 
@@ -457,6 +510,10 @@ def main():
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
                "note": "prefill flops over the whole step incl. decode and host copies"}
 
+    extras = None
+    if not args.no_extras and args.only == "all":
+        extras = time_extras(cga, dev, stream, flush_l2, args.steps)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         r = oracle_sample(args.cpu_seconds)
@@ -503,6 +560,7 @@ def main():
                          if args.prefill_batch is None and args.prefill_seq is None else None,
                          "kernel": "prefill_tc_kernel", "peak_source": pk["source"]},
             "e2e": e2e,
+            "extras": extras,
             "cpu_baseline": cpu,
             "clocks": clocks,
             "gpu_launches": 3 * args.steps,

@@ -65,6 +65,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_prefill_varlen.argtypes = [_dp, _dp, _dp, _i32p, _dp, _dp, ctypes.c_int,
                                           ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_double, ctypes.c_int, ctypes.c_int]
+    lib.oracle_rope_rows.restype = None
+    lib.oracle_rope_rows.argtypes = [_dp, _dp, _dp, _dp, ctypes.c_int64, ctypes.c_int]
     lib.oracle_row_partial.restype = None
     lib.oracle_row_partial.argtypes = [_dp, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_double,
                                        _dp, _dp, _dp]
@@ -193,6 +195,46 @@ def prefill_varlen(q, k, v, seqlens, causal: bool, scale: float, nthreads: int =
     if rc != 0:
         raise ValueError("oracle_prefill_varlen rejected its arguments")
     return o, lse
+
+
+def rope(x, cos_rows, sin_rows, lib=None):
+    """Rotate-half RoPE of x [..., D] with per-row tables cos/sin [..., D/2] (same leading
+    shape). fp64."""
+    lib = lib or load()
+    x = _f64(x)
+    c = np.ascontiguousarray(np.broadcast_to(_f64(cos_rows), x.shape[:-1] + (x.shape[-1] // 2,)))
+    sn = np.ascontiguousarray(np.broadcast_to(_f64(sin_rows), x.shape[:-1] + (x.shape[-1] // 2,)))
+    out = np.empty_like(x)
+    lib.oracle_rope_rows(_p(x), _p(c), _p(sn), _p(out), x.size // x.shape[-1], x.shape[-1])
+    return out
+
+
+def decode_rope(q, k_new, v_new, cos_tab, sin_tab, kcache, vcache, seqlens, scale: float,
+                lib=None):
+    """One decode step with the new token's RoPE and cache store: q [B,Hq,D] and k_new
+    [B,Hkv,D] are rotated at position p = seqlens[b]-1 with tables cos/sin [max_len, D/2]; the
+    rotated k (rounded to the cache's bf16) and v_new go to cache row p; then decode.
+    Returns (o [B,Hq,D], lse [B,Hq], k_row [B,Hkv,D] as stored) in float64."""
+    import torch
+
+    if hasattr(seqlens, "detach"):
+        seqlens = seqlens.detach().to("cpu").numpy()
+    sl = np.asarray(seqlens, dtype=np.int64)
+    qd, kd = _f64(q), _f64(k_new)
+    ct, st = _f64(cos_tab), _f64(sin_tab)
+    B, Hq, D = qd.shape
+    Hkv = kd.shape[1]
+    pos = np.maximum(sl - 1, 0)
+    q_rot = rope(qd, ct[pos][:, None, :], st[pos][:, None, :], lib=lib)
+    k_rot = rope(kd, ct[pos][:, None, :], st[pos][:, None, :], lib=lib)
+    k_store = torch.from_numpy(k_rot).to(torch.bfloat16).double().numpy()
+    kc, vc = _f64(kcache).copy(), _f64(vcache).copy()
+    for b in range(B):
+        if sl[b] > 0:
+            kc[b, :, pos[b]] = k_store[b]
+            vc[b, :, pos[b]] = _f64(v_new)[b]
+    o, lse = decode(q_rot, kc, vc, sl.astype(np.int32), scale, lib=lib)
+    return o, lse, k_store
 
 
 def row_partial(q_row, k_rows, v_rows, scale: float, lib=None):

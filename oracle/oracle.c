@@ -257,6 +257,27 @@ int oracle_prefill_varlen(const double *q, const double *k, const double *v, con
     return bad;
 }
 
+/* Rotary position embedding, rotate-half form, on n rows of D values (D even): with
+ * x = [x1 | x2] (halves of D/2), out = [x1*cos - x2*sin | x1*sin + x2*cos], cos and sin given per
+ * row as tables of D/2 values ("triton-optimization" skill, section 3.4: RoPE on the two halves
+ * of each head with precomputed cos/sin tables; "Hand-written Triton decoder", section 1.2: RoPE
+ * computed in floating point while loading q and k). */
+void oracle_rope_rows(const double *x, const double *cosv, const double *sinv, double *out,
+                      int64_t n, int D)
+{
+    const int H = D / 2;
+    for (int64_t r = 0; r < n; ++r) {
+        const double *xr = x + r * D;
+        const double *c = cosv + r * H;
+        const double *sn = sinv + r * H;
+        double *o = out + r * D;
+        for (int d = 0; d < H; ++d) {
+            o[d] = xr[d] * c[d] - xr[d + H] * sn[d];
+            o[d + H] = xr[d] * sn[d] + xr[d + H] * c[d];
+        }
+    }
+}
+
 /* ---- the method: online softmax over key blocks, and the merge of block partials ---- */
 
 /* Partial state of one query row over n keys (one block): m = max score, l = sum of

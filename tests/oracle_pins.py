@@ -331,9 +331,55 @@ def pin_varlen_is_prefill_of_each_sequence(lib):
         assert np.array_equal(of, op) and np.array_equal(lf, lp)
 
 
+def _rope_tables(n_pos, D, base=10000.0):
+    inv = base ** (-np.arange(D // 2) * 2.0 / D)
+    ang = np.arange(n_pos)[:, None] * inv[None, :]
+    return np.cos(ang), np.sin(ang)
+
+
+def pin_rope_closed_forms(lib):
+    """Rotate-half RoPE: a 2-D example worked by hand, norms preserved, identity at angle 0,
+    and q.k depends only on the position difference for a real RoPE table."""
+    th = 0.7
+    out = oracle.rope(np.array([[1.0, 0.0], [0.0, 1.0]]), np.array([[math.cos(th)]] * 2),
+                      np.array([[math.sin(th)]] * 2), lib=lib)
+    _close(out, np.array([[math.cos(th), math.sin(th)], [-math.sin(th), math.cos(th)]]), 1e-15,
+           "hand rotation")
+    rng = _rng(13)
+    D = 16
+    x = rng.standard_normal((5, D))
+    c, sn = _rope_tables(64, D)
+    rx = oracle.rope(x, c[7], sn[7], lib=lib)
+    _close(np.linalg.norm(rx, axis=-1), np.linalg.norm(x, axis=-1), 1e-12, "norm")
+    _close(oracle.rope(x, np.ones(D // 2), np.zeros(D // 2), lib=lib), x, 0.0, "identity")
+    q, k = rng.standard_normal(D), rng.standard_normal(D)
+    dots = [oracle.rope(q[None], c[p + 9], sn[p + 9], lib=lib)[0]
+            @ oracle.rope(k[None], c[p], sn[p], lib=lib)[0] for p in (0, 5, 30)]
+    _close(np.array(dots), np.full(3, dots[0]), 1e-12, "relative position")
+
+
+def pin_decode_rope_composition(lib):
+    """With identity tables the step is: store k_new, v_new at row L-1, then plain decode."""
+    rng = _rng(14)
+    B, Hq, Hkv, D, max_len = 2, 4, 2, 8, 12
+    q = rng.standard_normal((B, Hq, D)); kn = rng.standard_normal((B, Hkv, D))
+    vn = rng.standard_normal((B, Hkv, D))
+    kc = rng.standard_normal((B, Hkv, max_len, D)); vc = rng.standard_normal((B, Hkv, max_len, D))
+    ones, zeros = np.ones((max_len, D // 2)), np.zeros((max_len, D // 2))
+    o, lse, kst = oracle.decode_rope(q, kn, vn, ones, zeros, kc, vc, [12, 5], 0.5, lib=lib)
+    import torch
+    kb = torch.from_numpy(kn).to(torch.bfloat16).double().numpy()
+    kc2, vc2 = kc.copy(), vc.copy()
+    kc2[0, :, 11] = kb[0]; vc2[0, :, 11] = vn[0]
+    kc2[1, :, 4] = kb[1]; vc2[1, :, 4] = vn[1]
+    o2, lse2 = oracle.decode(q, kc2, vc2, [12, 5], 0.5, lib=lib)
+    _close(o, o2, 1e-14, "rope step O"); _close(lse, lse2, 1e-14, "rope step lse")
+
+
 ALL_PINS = [pin_rows_of_p_sum_to_one, pin_constant_keys_give_prefix_means,
             pin_single_key_returns_v, pin_two_keys_closed_form, pin_shift_invariance,
             pin_gqa_equals_repeated_heads, pin_brute_force_tiny, pin_merge_is_order_free,
             pin_online_equals_two_pass, pin_decode_is_last_prefill_row, pin_empty_decode_row,
             pin_hard_max_limit, pin_chunk_reduces_to_prefill_and_decode,
-            pin_varlen_is_prefill_of_each_sequence]
+            pin_varlen_is_prefill_of_each_sequence, pin_rope_closed_forms,
+            pin_decode_rope_composition]

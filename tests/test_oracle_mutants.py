@@ -43,6 +43,10 @@ MUTANTS = [
      "const long long p = (long long)i;"),
     ("varlen_padding_rows_live", "vis[j] = (i < L) && (causal ? (j <= i) : 1);",
      "vis[j] = (causal ? (j <= i) : 1);"),
+    ("rope_sign_swapped", "o[d] = xr[d] * c[d] - xr[d + H] * sn[d];",
+     "o[d] = xr[d] * c[d] + xr[d + H] * sn[d];"),
+    ("rope_halves_mixed", "o[d + H] = xr[d] * sn[d] + xr[d + H] * c[d];",
+     "o[d + H] = xr[d + H] * sn[d] + xr[d] * c[d];"),
     ("chunk_strict_causal", "vis[j] = causal ? ((long long)j <= p) : 1;",
      "vis[j] = causal ? ((long long)j < p) : 1;"),
 ]
