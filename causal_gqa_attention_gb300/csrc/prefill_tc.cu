@@ -118,6 +118,15 @@ __device__ __forceinline__ uint32_t too_big_for_f16(uint32_t w)
     return (uint32_t)((w & 0x7FFF0000u) >= 0x47800000u) | (uint32_t)((w & 0x7FFFu) >= 0x4780u);
 }
 
+// Zeroes rows >= rows_ok of a 128 x 128 bf16 tile: the 16-byte chunks ct, ct + 64, ... only.
+// Out of line on purpose: inlined (or folded into the conversion loop as a per-chunk select) it
+// cost the whole kernel 2-12% on full-length prefill, where it never runs.
+__device__ __noinline__ void zero_v_tail(uint4 *tile, int ct, int rows_ok)
+{
+    for (int c = ct; c < (int)(kTile / 16); c += 64)
+        if (((c & 1023) >> 3) >= rows_ok) tile[c] = make_uint4(0, 0, 0, 0);
+}
+
 // SPLIT = false: one block per (row block, head, batch), final O and LSE.
 // SPLIT = true: one block per (row block, key segment of J tiles, head, batch); it writes the
 // segment's normalised O (fp32) and its LSE (log2 units) to ws_o / ws_lse, and
@@ -327,13 +336,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!__all_sync(0xffffffffu, mbar_wait(&bar[B_VFULL + s], (jj / VST) & 1, abort_flag)))
                 break;
             uint4 *tile = reinterpret_cast<uint4 *>(smem + kOffV + s * kTile);
-            // rows at or past L (a cache's stale rows may hold anything) become 0: p is 0
-            // there, but 0 * NaN would not be
-            const int rows_ok = L - (jb + jj) * BN;
+            // rows at or past L (a cache's stale rows may hold anything) become 0 first: p is
+            // 0 there, but 0 * NaN would not be. Each thread zeroes only the chunks it converts
+            // below, so program order is the only ordering needed.
+            const int rows_ok = L - (jb + jj) * BN;  // >= BN except on the tile holding L
+            if (rows_ok < BN) zero_v_tail(tile, ct, rows_ok);
 #pragma unroll 4
             for (int c = ct; c < (int)(kTile / 16); c += 64) {
                 uint4 w = tile[c];
-                if (((c & 1023) >> 3) >= rows_ok) w = make_uint4(0, 0, 0, 0);
                 // |bf16| >= 2^16 (magnitude bits >= 0x4780) does not fit fp16; inf, NaN too
                 over |= too_big_for_f16(w.x) | too_big_for_f16(w.y) | too_big_for_f16(w.z) |
                         too_big_for_f16(w.w);
