@@ -23,7 +23,7 @@ from ._lib import (ATTN_BF16, ATTN_DEV_FP16_RANGE, ATTN_DEV_SEQLEN_CLAMPED, ATTN
 
 __all__ = [
     "attn_prefill", "attn_prefill_ex", "attn_prefill_varlen", "prefill_varlen", "attn_chunk", "attn_decode", "attn_decode_ex",
-    "attn_decode_noalloc", "chunk",
+    "attn_decode_noalloc", "chunk", "attn_decode_rope", "decode_rope",
     "attn_decode_workspace_bytes", "attn_decode_chunk_len", "attn_reserve_workspace",
     "attn_device_status", "attn_status_string", "attn_version", "prefill", "decode",
     "device_status", "AttnError", "ATTN_OK", "ATTN_ERR_INVALID", "ATTN_ERR_UNSUPPORTED",
@@ -70,6 +70,12 @@ def attn_decode_ex(q, kcache, vcache, seqlens, o, lse, B, Hq, Hkv, D, max_len, s
                    workspace_bytes, out_dtype, stream):
     return _lib.load().attn_decode_ex(q, kcache, vcache, seqlens, o, lse, B, Hq, Hkv, D, max_len,
                                       scale, workspace, workspace_bytes, out_dtype, stream)
+
+
+def attn_decode_rope(q, k_new, v_new, cos_t, sin_t, kcache, vcache, seqlens, o, lse, B, Hq, Hkv,
+                     D, max_len, scale, out_dtype, stream):
+    return _lib.load().attn_decode_rope(q, k_new, v_new, cos_t, sin_t, kcache, vcache, seqlens, o,
+                                        lse, B, Hq, Hkv, D, max_len, scale, out_dtype, stream)
 
 
 def attn_decode_noalloc(q, kcache, vcache, seqlens, o, lse, B, Hq, Hkv, D, max_len, scale,
@@ -271,6 +277,43 @@ def decode(q, kcache, vcache, seqlens, scale: float | None = None, out_dtype=Non
                             _ptr(lse), B, Hq, Hkv, D, max_len, float(scale), ws_ptr, ws_bytes,
                             out_t, _stream_handle(q.device))
     _lib.check("attn_decode_ex", rc)
+    return (out, lse) if return_lse else out
+
+
+def decode_rope(q, k_new, v_new, cos_t, sin_t, kcache, vcache, seqlens,
+                scale: float | None = None, out_dtype=None, return_lse: bool = False, out=None,
+                lse=None):
+    """Decode step with the new token's RoPE and cache store: q [B,Hq,D], k_new/v_new [B,Hkv,D]
+    bf16 (not rotated), cos_t/sin_t [max_len, D/2] fp32, caches [B,Hkv,max_len,D] bf16 (row
+    seqlens[b]-1 is written), seqlens [B] int32 (device, including the new token)."""
+    torch = _torch()
+    B, Hq, D = q.shape
+    Hkv, max_len = kcache.shape[1], kcache.shape[2]
+    if kcache.shape != (B, Hkv, max_len, D) or vcache.shape != kcache.shape:
+        raise ValueError("cache shapes do not match q")
+    if k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D):
+        raise ValueError("k_new/v_new must be [B, Hkv, D]")
+    if cos_t.shape != (max_len, D // 2) or sin_t.shape != cos_t.shape:
+        raise ValueError("cos/sin tables must be [max_len, D/2]")
+    for n, t in (("q", q), ("k_new", k_new), ("v_new", v_new), ("kcache", kcache),
+                 ("vcache", vcache)):
+        _check_cuda(n, t, torch.bfloat16)
+    _check_cuda("cos_t", cos_t, torch.float32)
+    _check_cuda("sin_t", sin_t, torch.float32)
+    _check_cuda("seqlens", seqlens, torch.int32)
+    out_dtype = out_dtype or torch.bfloat16
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=out_dtype, device=q.device)
+    if return_lse and lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    out_t = ATTN_BF16 if out_dtype == torch.bfloat16 else ATTN_F32
+    with torch.cuda.device(q.device):
+        rc = attn_decode_rope(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(cos_t), _ptr(sin_t),
+                              _ptr(kcache), _ptr(vcache), _ptr(seqlens), _ptr(out), _ptr(lse), B,
+                              Hq, Hkv, D, max_len, float(scale), out_t, _stream_handle(q.device))
+    _lib.check("attn_decode_rope", rc)
     return (out, lse) if return_lse else out
 
 

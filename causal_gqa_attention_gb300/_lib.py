@@ -40,6 +40,8 @@ SIGNATURES = {
     "attn_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]),
     "attn_decode_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _sz, _i,
                             _vp]),
+    "attn_decode_rope": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i,
+                              _i, _f, _i, _vp]),
     "attn_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp]),
     "attn_decode_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "attn_decode_chunk_len": (_i, [_i, _i, _i]),

@@ -363,6 +363,48 @@ int attn_decode_ex(const void *q, const void *kcache, const void *vcache, const 
     return cuda_status(gqa::launch_decode(a, out_dtype == ATTN_F32, st));
 }
 
+int attn_decode_rope(const void *q, const void *k_new, const void *v_new, const float *cos_t,
+                     const float *sin_t, void *kcache, void *vcache, const int *seqlens, void *o,
+                     float *lse, int B, int Hq, int Hkv, int D, int max_len, float scale,
+                     int out_dtype, void *stream)
+{
+    int rc = check_decode(q, kcache, vcache, seqlens, o, lse, B, Hq, Hkv, D, max_len, scale,
+                          out_dtype);
+    if (rc != ATTN_OK) return rc;
+    if (!k_new || !v_new || !cos_t || !sin_t) return ATTN_ERR_INVALID;
+    if (!aligned4(cos_t) || !aligned4(sin_t) || (reinterpret_cast<uintptr_t>(k_new) & 1u) ||
+        (reinterpret_cast<uintptr_t>(v_new) & 1u))
+        return ATTN_ERR_ALIGN;
+    const size_t dec = (gqa::decode_workspace_bytes(B, Hq, Hkv, D, max_len) + 255) & ~(size_t)255;
+    const size_t need = dec + (size_t)B * Hq * D * sizeof(float);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    void *ws = nullptr;
+    rc = workspace_acquire(need, st, true, &ws);
+    if (rc != ATTN_OK) return rc;
+    float *q_rot = reinterpret_cast<float *>(static_cast<char *>(ws) + dec);
+    rc = cuda_status(gqa::launch_rope_append(q, k_new, v_new, cos_t, sin_t, kcache, vcache,
+                                             seqlens, q_rot, B, Hq, Hkv, D, max_len, st));
+    if (rc != ATTN_OK) return rc;
+    DecodeArgs a;
+    a.q = q_rot;
+    a.q_f32 = true;
+    a.kc = kcache;
+    a.vc = vcache;
+    a.seqlens = seqlens;
+    a.o = o;
+    a.lse = lse;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.max_len = max_len;
+    a.ws = ws;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    rc = status_ptr(&a.status);
+    if (rc != ATTN_OK) return rc;
+    return cuda_status(gqa::launch_decode(a, out_dtype == ATTN_F32, st));
+}
+
 int attn_decode(const void *q, const void *kcache, const void *vcache, const int *seqlens,
                 void *o, int B, int Hq, int Hkv, int D, int max_len, float scale, void *stream)
 {

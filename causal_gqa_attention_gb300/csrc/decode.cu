@@ -187,24 +187,34 @@ __device__ __forceinline__ void group_sums(const float (&l_own)[Plan<D, HG>::NV]
     }
 }
 
-// q fragment (8 dims of each of the HG heads starting at h0), scaled to log2 units.
-template <int D, int HG>
-__device__ __forceinline__ void load_q(const __nv_bfloat16 *q, size_t row0, int gl,
-                                       float scale_log2, float2 (&qp)[HG][4])
+// q fragment (8 dims of each of the HG heads starting at h0), scaled to log2 units. q is bf16,
+// or fp32 when it comes from the RoPE step (kept unrounded).
+template <int D, int HG, typename QT>
+__device__ __forceinline__ void load_q(const QT *q, size_t row0, int gl, float scale_log2,
+                                       float2 (&qp)[HG][4])
 {
 #pragma unroll
     for (int h = 0; h < HG; ++h) {
-        const uint4 w = *reinterpret_cast<const uint4 *>(q + (row0 + h) * D + gl * 8);
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        if constexpr (sizeof(QT) == 4) {
+            const float4 *src = reinterpret_cast<const float4 *>(q + (row0 + h) * D + gl * 8);
+            const float4 a = src[0], c = src[1];
+            qp[h][0] = make_float2(a.x * scale_log2, a.y * scale_log2);
+            qp[h][1] = make_float2(a.z * scale_log2, a.w * scale_log2);
+            qp[h][2] = make_float2(c.x * scale_log2, c.y * scale_log2);
+            qp[h][3] = make_float2(c.z * scale_log2, c.w * scale_log2);
+        } else {
+            const uint4 w = *reinterpret_cast<const uint4 *>(q + (row0 + h) * D + gl * 8);
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-            qp[h][e] = make_float2(bf16lo(ws[e]) * scale_log2, bf16hi(ws[e]) * scale_log2);
+            for (int e = 0; e < 4; ++e)
+                qp[h][e] = make_float2(bf16lo(ws[e]) * scale_log2, bf16hi(ws[e]) * scale_log2);
+        }
     }
 }
 
-template <int D, int HG>
+template <int D, int HG, typename QT>
 __global__ void __launch_bounds__(kWarps * 32)
-    decode_split_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ kc,
+    decode_split_kernel(const QT *__restrict__ q, const __nv_bfloat16 *__restrict__ kc,
                         const __nv_bfloat16 *__restrict__ vc, const int *__restrict__ seqlens,
                         float *__restrict__ ws_o, float2 *__restrict__ ws_ml, int Hq, int Hkv,
                         int max_len, int chunk, int nsplit, float scale_log2,
@@ -219,6 +229,9 @@ __global__ void __launch_bounds__(kWarps * 32)
                                                   P::PBUF);
     float *comb = reinterpret_cast<float *>(smem);  // reuses the ring after the last stage
 
+    // launched as a programmatic dependent: nothing from global memory is read before the
+    // previous kernel in the stream has finished and flushed
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int split = blockIdx.x;
     const int subgroups = gridDim.y / Hkv;
     const int g = blockIdx.y / subgroups;
@@ -265,7 +278,7 @@ __global__ void __launch_bounds__(kWarps * 32)
             if (warp + r * kWarps < nstage) issue(warp + r * kWarps);
 
     float2 qp[HG][4];
-    load_q<D, HG>(q, (size_t)b * Hq + h0, gl, scale_log2, qp);
+    load_q<D, HG, QT>(q, (size_t)b * Hq + h0, gl, scale_log2, qp);
 
     float m_ref[HG];       // running max reference per head (uniform over the group)
     float2 acc[HG][4];     // unnormalised output, this lane's 8 dims of each head
@@ -403,9 +416,9 @@ __device__ __forceinline__ void cursor_advance(StreamCursor &c, int n, const int
     }
 }
 
-template <int D, int HG>
+template <int D, int HG, typename QT>
 __global__ void __launch_bounds__(kWarps * 32)
-    decode_stream_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ kc,
+    decode_stream_kernel(const QT *__restrict__ q, const __nv_bfloat16 *__restrict__ kc,
                          const __nv_bfloat16 *__restrict__ vc, const int *__restrict__ seqlens,
                          float *__restrict__ ws_o, float2 *__restrict__ ws_ml, int B, int Hq,
                          int Hkv, int max_len, float scale_log2, unsigned *__restrict__ status)
@@ -430,6 +443,9 @@ __global__ void __launch_bounds__(kWarps * 32)
         fence_mbar_init();
     }
     __syncthreads();
+    // launched as a programmatic dependent: nothing from global memory is read before the
+    // previous kernel in the stream has finished and flushed
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // ---- this warp's slice of the key list
     bool bad = false;
@@ -512,7 +528,7 @@ __global__ void __launch_bounds__(kWarps * 32)
             const bool last = (cc.off + n == cc.Lb) || (cc.pos + n == r1);
             if (first) {
                 const int g = cc.sl / SUB, gs = cc.sl % SUB;
-                load_q<D, HG>(q, (size_t)cc.b * Hq + g * G + gs * HG, gl, scale_log2, qp);
+                load_q<D, HG, QT>(q, (size_t)cc.b * Hq + g * G + gs * HG, gl, scale_log2, qp);
 #pragma unroll
                 for (int h = 0; h < HG; ++h) {
                     m_ref[h] = -INFINITY;
@@ -787,7 +803,26 @@ cudaError_t launch_merge(const DecodeArgs &a, cudaStream_t st)
                               a.chunk, a.nsplit);
 }
 
-template <int D, int HG>
+// Launch as a programmatic dependent of whatever precedes it in the stream (the kernels wait
+// for it before their first global read, so only their start-up overlaps it).
+template <typename K, typename... Args>
+cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+template <int D, int HG, typename QT>
 cudaError_t launch_split_t(const DecodeArgs &a, cudaStream_t st)
 {
     using P = Plan<D, HG>;
@@ -796,18 +831,17 @@ cudaError_t launch_split_t(const DecodeArgs &a, cudaStream_t st)
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 64 || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(decode_split_kernel<D, HG>,
+        e = cudaFuncSetAttribute(decode_split_kernel<D, HG, QT>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM);
         if (e != cudaSuccess) return e;
         if (dev < 64) attr_set[dev] = true;
     }
     const int G = a.Hq / a.Hkv;
     dim3 grid(a.nsplit, a.Hkv * (G / HG), a.B);
-    decode_split_kernel<D, HG><<<grid, kWarps * 32, P::SMEM, st>>>(
-        static_cast<const __nv_bfloat16 *>(a.q), static_cast<const __nv_bfloat16 *>(a.kc),
-        static_cast<const __nv_bfloat16 *>(a.vc), a.seqlens, a.ws_o, a.ws_ml, a.Hq, a.Hkv,
-        a.max_len, a.chunk, a.nsplit, a.scale_log2, a.status);
-    return cudaGetLastError();
+    return launch_pdl(decode_split_kernel<D, HG, QT>, grid, dim3(kWarps * 32), P::SMEM, st,
+                      static_cast<const QT *>(a.q), static_cast<const __nv_bfloat16 *>(a.kc),
+                      static_cast<const __nv_bfloat16 *>(a.vc), a.seqlens, a.ws_o, a.ws_ml,
+                      a.Hq, a.Hkv, a.max_len, a.chunk, a.nsplit, a.scale_log2, a.status);
 }
 
 int largest_group(int G)
@@ -815,7 +849,7 @@ int largest_group(int G)
     return G % 8 == 0 ? 8 : (G % 4 == 0 ? 4 : (G % 2 == 0 ? 2 : 1));
 }
 
-template <int D, int HG>
+template <int D, int HG, typename QT>
 cudaError_t launch_stream_t(const DecodeArgs &a, bool out_f32, cudaStream_t st)
 {
     using P = Plan<D, HG>;
@@ -826,13 +860,13 @@ cudaError_t launch_stream_t(const DecodeArgs &a, bool out_f32, cudaStream_t st)
     if (e != cudaSuccess) return e;
     int blocks = dev < 64 ? blocks_cached[dev] : 0;
     if (dev >= 64 || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(decode_stream_kernel<D, HG>,
+        e = cudaFuncSetAttribute(decode_stream_kernel<D, HG, QT>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, P::RING + P::PBUF + P::BARS);
         if (e != cudaSuccess) return e;
         int sms = 0, occ = 0;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_stream_kernel<D, HG>,
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_stream_kernel<D, HG, QT>,
                                                           kWarps * 32, P::RING + P::PBUF + P::BARS);
         if (e != cudaSuccess) return e;
         blocks = sms * (occ > 0 ? occ : 1);
@@ -845,11 +879,11 @@ cudaError_t launch_stream_t(const DecodeArgs &a, bool out_f32, cudaStream_t st)
     float *ws_o = static_cast<float *>(a.ws);
     const size_t rows = (size_t)kStreamMaxWarps * HG + (size_t)a.B * a.Hq;
     float2 *ws_ml = reinterpret_cast<float2 *>(ws_o + rows * D);
-    decode_stream_kernel<D, HG><<<blocks, kWarps * 32, P::RING + P::PBUF + P::BARS, st>>>(
-        static_cast<const __nv_bfloat16 *>(a.q), static_cast<const __nv_bfloat16 *>(a.kc),
-        static_cast<const __nv_bfloat16 *>(a.vc), a.seqlens, ws_o, ws_ml, a.B, a.Hq, a.Hkv,
-        a.max_len, a.scale_log2, a.status);
-    e = cudaGetLastError();
+    e = launch_pdl(decode_stream_kernel<D, HG, QT>, dim3(blocks), dim3(kWarps * 32),
+                   P::RING + P::PBUF + P::BARS, st, static_cast<const QT *>(a.q),
+                   static_cast<const __nv_bfloat16 *>(a.kc),
+                   static_cast<const __nv_bfloat16 *>(a.vc), a.seqlens, ws_o, ws_ml, a.B, a.Hq,
+                   a.Hkv, a.max_len, a.scale_log2, a.status);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.B * a.Hq);
@@ -870,26 +904,63 @@ cudaError_t launch_stream_t(const DecodeArgs &a, bool out_f32, cudaStream_t st)
                               a.max_len, nwt);
 }
 
-template <int D>
+template <int D, typename QT>
 cudaError_t launch_stream_d(const DecodeArgs &a, bool out_f32, cudaStream_t st)
 {
     switch (largest_group(a.Hq / a.Hkv)) {
-    case 8: return launch_stream_t<D, 8>(a, out_f32, st);
-    case 4: return launch_stream_t<D, 4>(a, out_f32, st);
-    case 2: return launch_stream_t<D, 2>(a, out_f32, st);
-    default: return launch_stream_t<D, 1>(a, out_f32, st);
+    case 8: return launch_stream_t<D, 8, QT>(a, out_f32, st);
+    case 4: return launch_stream_t<D, 4, QT>(a, out_f32, st);
+    case 2: return launch_stream_t<D, 2, QT>(a, out_f32, st);
+    default: return launch_stream_t<D, 1, QT>(a, out_f32, st);
     }
 }
 
-template <int D>
+template <int D, typename QT>
 cudaError_t launch_split_d(const DecodeArgs &a, cudaStream_t st)
 {
     switch (largest_group(a.Hq / a.Hkv)) {
-    case 8: return launch_split_t<D, 8>(a, st);
-    case 4: return launch_split_t<D, 4>(a, st);
-    case 2: return launch_split_t<D, 2>(a, st);
-    default: return launch_split_t<D, 1>(a, st);
+    case 8: return launch_split_t<D, 8, QT>(a, st);
+    case 4: return launch_split_t<D, 4, QT>(a, st);
+    case 2: return launch_split_t<D, 2, QT>(a, st);
+    default: return launch_split_t<D, 1, QT>(a, st);
     }
+}
+
+// RoPE of the new token and its cache store. One block per (sequence, head): blockIdx.y < Hq
+// rotates query head y into q_rot (fp32, unrounded); otherwise kv head y - Hq: its key is
+// rotated, rounded to bf16 and stored with its value at cache row p = seqlens[b] - 1. Thread d
+// handles the pair (d, d + D/2): [x1 | x2] -> [x1 cos - x2 sin | x1 sin + x2 cos].
+template <int D>
+__global__ void __launch_bounds__(D / 2)
+    rope_append_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k_new,
+                       const __nv_bfloat16 *__restrict__ v_new, const float *__restrict__ cos_t,
+                       const float *__restrict__ sin_t, __nv_bfloat16 *__restrict__ kc,
+                       __nv_bfloat16 *__restrict__ vc, const int *__restrict__ seqlens,
+                       float *__restrict__ q_rot, int Hq, int Hkv, int max_len)
+{
+    constexpr int H = D / 2;
+    const int b = blockIdx.x, y = blockIdx.y, d = threadIdx.x;
+    const int L = clamp_len(seqlens[b], max_len);
+    const int p = L > 0 ? L - 1 : 0;
+    const float c = cos_t[(size_t)p * H + d], sn = sin_t[(size_t)p * H + d];
+    if (y < Hq) {
+        const __nv_bfloat16 *x = q + ((size_t)b * Hq + y) * D;
+        const float x1 = __bfloat162float(x[d]), x2 = __bfloat162float(x[d + H]);
+        float *o = q_rot + ((size_t)b * Hq + y) * D;
+        o[d] = x1 * c - x2 * sn;
+        o[d + H] = x1 * sn + x2 * c;
+    } else if (L > 0) {
+        const int g = y - Hq;
+        const __nv_bfloat16 *x = k_new + ((size_t)b * Hkv + g) * D;
+        const float x1 = __bfloat162float(x[d]), x2 = __bfloat162float(x[d + H]);
+        const size_t row = (((size_t)b * Hkv + g) * max_len + p) * D;
+        kc[row + d] = __float2bfloat16_rn(x1 * c - x2 * sn);
+        kc[row + d + H] = __float2bfloat16_rn(x1 * sn + x2 * c);
+        const __nv_bfloat16 *vn = v_new + ((size_t)b * Hkv + g) * D;
+        vc[row + d] = vn[d];
+        vc[row + d + H] = vn[d + H];
+    }
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 }  // namespace
@@ -922,19 +993,50 @@ size_t decode_workspace_bytes(int B, int Hq, int Hkv, int D, int max_len)
 cudaError_t launch_decode(const DecodeArgs &a0, bool out_f32, cudaStream_t st)
 {
     DecodeArgs a = a0;
-    if (a.B <= kStreamMaxBatch)
-        return a.D == 128 ? launch_stream_d<128>(a, out_f32, st) : launch_stream_d<64>(a, out_f32, st);
+    if (a.B <= kStreamMaxBatch) {
+        if (a.q_f32)
+            return a.D == 128 ? launch_stream_d<128, float>(a, out_f32, st)
+                              : launch_stream_d<64, float>(a, out_f32, st);
+        return a.D == 128 ? launch_stream_d<128, __nv_bfloat16>(a, out_f32, st)
+                          : launch_stream_d<64, __nv_bfloat16>(a, out_f32, st);
+    }
     a.chunk = decode_chunk_len(a.B, a.Hkv, a.max_len);
     a.nsplit = (a.max_len + a.chunk - 1) / a.chunk;
     a.ws_o = static_cast<float *>(a.ws);
     a.ws_ml = reinterpret_cast<float2 *>(a.ws_o + (size_t)a.B * a.Hq * a.nsplit * a.D);
-    cudaError_t e = (a.D == 128) ? launch_split_d<128>(a, st) : launch_split_d<64>(a, st);
+    cudaError_t e;
+    if (a.q_f32)
+        e = (a.D == 128) ? launch_split_d<128, float>(a, st) : launch_split_d<64, float>(a, st);
+    else
+        e = (a.D == 128) ? launch_split_d<128, __nv_bfloat16>(a, st)
+                         : launch_split_d<64, __nv_bfloat16>(a, st);
     if (e != cudaSuccess) return e;
     if (a.D == 128)
         e = out_f32 ? launch_merge<true, 128>(a, st) : launch_merge<false, 128>(a, st);
     else
         e = out_f32 ? launch_merge<true, 64>(a, st) : launch_merge<false, 64>(a, st);
     return e;
+}
+
+cudaError_t launch_rope_append(const void *q, const void *k_new, const void *v_new,
+                               const float *cos_t, const float *sin_t, void *kc, void *vc,
+                               const int *seqlens, float *q_rot, int B, int Hq, int Hkv, int D,
+                               int max_len, cudaStream_t st)
+{
+    dim3 grid(B, Hq + Hkv);
+    if (D == 128)
+        rope_append_kernel<128><<<grid, 64, 0, st>>>(
+            static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k_new),
+            static_cast<const __nv_bfloat16 *>(v_new), cos_t, sin_t,
+            static_cast<__nv_bfloat16 *>(kc), static_cast<__nv_bfloat16 *>(vc), seqlens, q_rot,
+            Hq, Hkv, max_len);
+    else
+        rope_append_kernel<64><<<grid, 32, 0, st>>>(
+            static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k_new),
+            static_cast<const __nv_bfloat16 *>(v_new), cos_t, sin_t,
+            static_cast<__nv_bfloat16 *>(kc), static_cast<__nv_bfloat16 *>(vc), seqlens, q_rot,
+            Hq, Hkv, max_len);
+    return cudaGetLastError();
 }
 
 }  // namespace gqa

@@ -55,12 +55,20 @@ struct DecodeArgs {
     int B, Hq, Hkv, D, max_len;
     float scale_log2;
     unsigned *status;
+    bool q_f32 = false;   // q is fp32 (the RoPE step's output) instead of bf16
     // filled in by launch_decode for the chunked kernel
     float *ws_o = nullptr;
     float2 *ws_ml = nullptr;
     int chunk = 0, nsplit = 0;
 };
 cudaError_t launch_decode(const DecodeArgs &a, bool out_f32, cudaStream_t stream);
+
+// RoPE (rotate-half) of the new token of each sequence at position seqlens[b] - 1: q into
+// q_rot [B, Hq, D] fp32; k_new rotated and v_new stored at that row of the caches.
+cudaError_t launch_rope_append(const void *q, const void *k_new, const void *v_new,
+                               const float *cos_t, const float *sin_t, void *kc, void *vc,
+                               const int *seqlens, float *q_rot, int B, int Hq, int Hkv, int D,
+                               int max_len, cudaStream_t stream);
 
 // Device address of the library's status word on the current device.
 int status_word_ptr(unsigned **out);

@@ -183,6 +183,29 @@ int attn_decode_noalloc(const void *q, const void *kcache, const void *vcache, c
                         void *o, float *lse, int B, int Hq, int Hkv, int D, int max_len,
                         float scale, int out_dtype, void *stream);
 
+/*
+ * attn_decode_rope -- one decode step that first places the new token: rotary position
+ * embedding (rotate-half form) of the new query and key at position p = seqlens[b] - 1, the
+ * rotated key (rounded to bf16) and the value stored at cache row p, then decode as attn_decode
+ * with the rotated query (kept in fp32, not rounded).
+ *   q      [B, Hq, D] bf16, not yet rotated     k_new, v_new [B, Hkv, D] bf16, k_new not rotated
+ *   cos_t, sin_t  [max_len, D/2] fp32 tables, row p used for position p:
+ *                 [x1 | x2] -> [x1 cos - x2 sin | x1 sin + x2 cos] on the two halves of a head
+ *   kcache, vcache [B, Hkv, max_len, D] bf16, row seqlens[b]-1 overwritten
+ *   seqlens [B] int32 (device): lengths including the new token
+ *   o [B, Hq, D] bf16 or fp32 by out_dtype, lse [B, Hq] fp32 or NULL
+ * Scratch (partials and the rotated queries) comes from the library-owned buffer, grown on
+ * first use as for attn_decode. Requires D in {64, 128}.
+ * Sources: "triton-optimization" skill (skillsmp.com) section 3.4 (RoPE on the two halves of a
+ * head with precomputed cos/sin tables, q and k in one kernel); "Hand-written Triton decoder"
+ * (m.nlpx.cn/news/28229) section 1.2 (RoPE computed in fp32 while q and k are loaded) and
+ * section 2.2 (RoPE and the KV-cache store are operators of the decode step).
+ */
+int attn_decode_rope(const void *q, const void *k_new, const void *v_new, const float *cos_t,
+                     const float *sin_t, void *kcache, void *vcache, const int *seqlens, void *o,
+                     float *lse, int B, int Hq, int Hkv, int D, int max_len, float scale,
+                     int out_dtype, void *stream);
+
 /* Workspace bytes attn_decode_ex needs for this shape (0 for invalid arguments).
  * Depends only on the arguments, not on the device. */
 size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int max_len);
