@@ -58,7 +58,7 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-extras", action="store_true",
-                   help="skip the extra timings (cache chunk, padded varlen prefill)")
+                   help="skip the extra timings (cache chunk, padded varlen prefill, decode with RoPE)")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle sample")
     p.add_argument("--only", default="all", choices=["all", "prefill", "decode"],
@@ -345,6 +345,28 @@ def time_extras(cga, dev, stream, flush, steps):
     fl = sum(workloads.prefill_flops(1, Hq, int(L), D, True) for L in lens.tolist())
     out["varlen_b8_s1024to8192_padded8192"] = {"ms": ms, "value": fl / (ms * 1e-3) / 1e12,
                                                "unit": "TFLOP/s", "flops": fl}
+    del q, k, v, o
+    # decode step with RoPE of the new token and its cache store (32 sequences of 256..4096),
+    # beside the plain decode of the same caches
+    cfg = workloads.CONFIGS["c4b"]
+    q, kc, vc, sl = [t.to(dev) for t in workloads.config_decode_inputs(cfg)]
+    Bd, Hkv, D = cfg.B, cfg.Hkv, cfg.D
+    k_new = torch.randn((Bd, Hkv, D), generator=g).to(torch.bfloat16).to(dev)
+    v_new = torch.randn((Bd, Hkv, D), generator=g).to(torch.bfloat16).to(dev)
+    inv = 10000.0 ** (-torch.arange(D // 2, dtype=torch.float64) * 2 / D)
+    ang = torch.arange(cfg.max_len, dtype=torch.float64)[:, None] * inv[None, :]
+    cos_t, sin_t = ang.cos().float().to(dev), ang.sin().float().to(dev)
+    o = torch.empty_like(q)
+    reps = max(3, steps // 2)
+    ms_rope = _time(lambda: cga.decode_rope(q, k_new, v_new, cos_t, sin_t, kc, vc, sl, out=o),
+                    flush, stream, reps)
+    ms_plain = _time(lambda: cga.decode(q, kc, vc, sl, out=o), flush, stream, reps)
+    lens = sl.cpu().tolist()
+    by = (workloads.decode_bytes(lens, cfg.Hq, Hkv, D) + 4 * Bd * Hkv * D * 2
+          + 2 * Bd * (D // 2) * 4)  # + k_new/v_new read and stored, + cos/sin rows
+    out["decode_rope_b32_l256to4096"] = {"ms": ms_rope, "value": by / (ms_rope * 1e-3) / 1e9,
+                                         "unit": "GB/s", "bytes": by,
+                                         "plain_decode_ms": ms_plain}
     return out
 
 
