@@ -22,7 +22,7 @@ from ._lib import (ATTN_BF16, ATTN_DEV_FP16_RANGE, ATTN_DEV_SEQLEN_CLAMPED, ATTN
                    ATTN_ERR_WORKSPACE, ATTN_F32, ATTN_OK, AttnError)
 
 __all__ = [
-    "attn_prefill", "attn_prefill_ex", "attn_prefill_varlen", "prefill_varlen", "attn_chunk", "attn_decode", "attn_decode_ex",
+    "attn_prefill", "attn_prefill_ex", "attn_prefill_strided", "attn_prefill_varlen", "prefill_varlen", "attn_chunk", "attn_decode", "attn_decode_ex",
     "attn_decode_noalloc", "chunk", "attn_decode_rope", "decode_rope",
     "attn_decode_workspace_bytes", "attn_decode_chunk_len", "attn_reserve_workspace",
     "attn_device_status", "attn_status_string", "attn_version", "prefill", "decode",
@@ -47,6 +47,13 @@ def attn_prefill_ex(q, k, v, o, lse, B, S, Hq, Hkv, D, scale, causal, in_dtype, 
                     stream):
     return _lib.load().attn_prefill_ex(q, k, v, o, lse, B, S, Hq, Hkv, D, scale, causal,
                                        in_dtype, out_dtype, stream)
+
+
+def attn_prefill_strided(q, k, v, o, lse, B, S, Hq, Hkv, D, q_strides, k_strides, v_strides,
+                         o_strides, scale, causal, out_dtype, stream):
+    return _lib.load().attn_prefill_strided(q, k, v, o, lse, B, S, Hq, Hkv, D, q_strides,
+                                            k_strides, v_strides, o_strides, scale, causal,
+                                            out_dtype, stream)
 
 
 def attn_prefill_varlen(q, k, v, seqlens, o, lse, B, S, Hq, Hkv, D, scale, causal, out_dtype,
@@ -137,14 +144,42 @@ def _check_cuda(name, t, dtype=None):
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
 
 
+def _bshd_strides(t):
+    """Element strides {batch, token, head} of a [B, H, S, D] view (head dim contiguous); a
+    dimension of extent 1 gets a nominal stride (it is never stepped)."""
+    import ctypes
+
+    sb, sh, ss = t.stride(0), t.stride(1), t.stride(2)
+    if t.shape[0] == 1:
+        sb = 8
+    if t.shape[1] == 1:
+        sh = 8
+    if t.shape[2] == 1:
+        ss = 8
+    return (ctypes.c_longlong * 3)(sb, ss, sh)
+
+
+def _check_view(name, t, dtype):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dim() != 4 or t.stride(3) != 1:
+        raise ValueError(f"{name} must be a 4-D view with a contiguous last dim")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
 def prefill(q, k, v, causal: bool = True, scale: float | None = None, out_dtype=None,
             return_lse: bool = False, out=None, lse=None):
     """Attention forward with q_len = kv_len.
 
-    q [B,Hq,S,D], k/v [B,Hkv,S,D], all bf16 (tensor-core path, D = 128) or all fp32 (fp32
+    q [B,Hq,S,D], k/v [B,Hkv,S,D], all bf16 (tensor-core path, D in {64,128}) or all fp32 (fp32
     CUDA-core path, D in {64,128}). ``out_dtype`` defaults to the input dtype (bf16 inputs may
     ask for fp32 output: the result before the final rounding). Returns o, or (o, lse) with
-    lse [B,Hq,S] fp32 (natural log)."""
+    lse [B,Hq,S] fp32 (natural log).
+
+    bf16 q, k, v (and ``out``) may be views with any strides as long as the head dim is
+    contiguous, e.g. ``x.transpose(1, 2)`` of a [B,S,H,D] tensor, or head slices of a fused QKV
+    projection output viewed as [B,S,Hq+2Hkv,D]: they are read and written in place."""
     torch = _torch()
     B, Hq, S, D = q.shape
     Hkv = k.shape[1]
@@ -152,19 +187,30 @@ def prefill(q, k, v, causal: bool = True, scale: float | None = None, out_dtype=
         raise ValueError(f"k/v shape {tuple(k.shape)}/{tuple(v.shape)} do not match q {tuple(q.shape)}")
     if q.dtype not in (torch.bfloat16, torch.float32):
         raise ValueError("q/k/v must be bf16 or fp32")
-    for n, t in (("q", q), ("k", k), ("v", v)):
-        _check_cuda(n, t, q.dtype)
     out_dtype = out_dtype or q.dtype
     if out is None:
         out = torch.empty((B, Hq, S, D), dtype=out_dtype, device=q.device)
-    else:
-        _check_cuda("out", out, out_dtype)
+    elif out.shape != (B, Hq, S, D):
+        raise ValueError(f"out must be [B,Hq,S,D], got {tuple(out.shape)}")
     if return_lse and lse is None:
         lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    in_t = ATTN_BF16 if q.dtype == torch.bfloat16 else ATTN_F32
     out_t = ATTN_BF16 if out_dtype == torch.bfloat16 else ATTN_F32
+    views = (("q", q, q.dtype), ("k", k, q.dtype), ("v", v, q.dtype), ("out", out, out_dtype))
+    if q.dtype == torch.bfloat16 and not all(t.is_contiguous() for _, t, _ in views):
+        for n, t, dt in views:
+            _check_view(n, t, dt)
+        with torch.cuda.device(q.device):
+            rc = attn_prefill_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, S, Hq,
+                                      Hkv, D, _bshd_strides(q), _bshd_strides(k),
+                                      _bshd_strides(v), _bshd_strides(out), float(scale),
+                                      int(bool(causal)), out_t, _stream_handle(q.device))
+        _lib.check("attn_prefill_strided", rc)
+        return (out, lse) if return_lse else out
+    for n, t, dt in views:
+        _check_cuda(n, t, dt)
+    in_t = ATTN_BF16 if q.dtype == torch.bfloat16 else ATTN_F32
     with torch.cuda.device(q.device):
         rc = attn_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, S, Hq, Hkv, D,
                              float(scale), int(bool(causal)), in_t, out_t,

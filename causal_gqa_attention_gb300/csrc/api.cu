@@ -43,18 +43,43 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// bf16 tensor viewed as [planes, rows, 128] with a 64 x 128-row box, 128-byte swizzle.
-bool encode_bf16_rows(CUtensorMap *m, const void *base, long long planes, long long rows)
+// Element strides of one [B, H, rows, D] operand: batch, row (token), head; the head dim is
+// contiguous.
+struct Strides {
+    long long b, s, h;
+};
+
+Strides contiguous(int H, long long rows, int D)
+{
+    return Strides{(long long)H * rows * D, D, rows * D};
+}
+
+// bf16 tensor viewed as {D, rows, heads, batch} with the given element strides, a 64-column x
+// 128-row box and 128-byte swizzle; reads past `rows` (or any extent) fill with zeros.
+bool encode_bf16_4d(CUtensorMap *m, const void *base, int D, long long rows, int heads, int batch,
+                    const Strides &st)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    const cuuint64_t dims[3] = {128, (cuuint64_t)rows, (cuuint64_t)planes};
-    const cuuint64_t strides[2] = {128 * 2, (cuuint64_t)rows * 128 * 2};  // bytes, dims 1..2
-    const cuuint32_t box[3] = {64, 128, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)heads,
+                                (cuuint64_t)batch};
+    const cuuint64_t strides[3] = {(cuuint64_t)st.s * 2, (cuuint64_t)st.h * 2,
+                                   (cuuint64_t)st.b * 2};  // bytes, dims 1..3
+    const cuuint32_t box[4] = {64, 128, 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Strides usable by the tensor maps (bf16 operands) or by the 16-byte output stores: positive,
+// below 2^39 elements, and a multiple of 16 bytes.
+bool strides_ok(const Strides &st, int elem_bytes)
+{
+    const long long v[3] = {st.b, st.s, st.h};
+    for (long long x : v)
+        if (x <= 0 || x >= (1LL << 39) || (x * elem_bytes) % 16 != 0) return false;
+    return true;
 }
 
 // ---- device status word address, per device
@@ -135,7 +160,7 @@ int check_prefill(const void *q, const void *k, const void *v, void *o, float *l
         return ATTN_ERR_INVALID;
     if ((long long)B * Hq > (1LL << 30) || (long long)B * Hq * S > (1LL << 40))
         return ATTN_ERR_UNSUPPORTED;
-    if (in_t == ATTN_BF16 && D != 128) return ATTN_ERR_UNSUPPORTED;
+    if (in_t == ATTN_BF16 && D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
     if (in_t == ATTN_BF16 && (long long)((S + 255) / 256) * B * Hq >= (1LL << 31))
         return ATTN_ERR_UNSUPPORTED;
     if (in_t == ATTN_F32 && ((D != 64 && D != 128) || out_t != ATTN_F32)) return ATTN_ERR_UNSUPPORTED;
@@ -161,6 +186,54 @@ int check_decode(const void *q, const void *kc, const void *vc, const int *seqle
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+// bf16 prefill on the tensor-core kernel for checked arguments and strides.
+int prefill_bf16(const void *q, const void *k, const void *v, void *o, float *lse, int B, int S,
+                 int Hq, int Hkv, int D, float scale, int causal, int out_dtype, const Strides &qs,
+                 const Strides &ks, const Strides &vs, const Strides &os, void *stream)
+{
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    PrefillTcArgs a;
+    std::memset(&a, 0, sizeof(a));
+    if (!encode_bf16_4d(&a.tq, q, D, S, Hq, B, qs) || !encode_bf16_4d(&a.tk, k, D, S, Hkv, B, ks) ||
+        !encode_bf16_4d(&a.tv, v, D, S, Hkv, B, vs))
+        return ATTN_ERR_CUDA;
+    a.o = o;
+    a.o_sb = os.b;
+    a.o_ss = os.s;
+    a.o_sh = os.h;
+    a.lse = lse;
+    a.B = B;
+    a.S = S;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.causal = causal ? 1 : 0;
+    int rc = status_ptr(&a.status);
+    if (rc != ATTN_OK) return rc;
+    // Small grids (fewer row blocks x heads than SMs) split the keys of each row block over
+    // several blocks and merge; the partials use the library-owned scratch. If that scratch
+    // cannot grow now (stream capture), the unsplit kernel runs instead.
+    int sms = 0;
+    rc = sm_count(&sms);
+    if (rc != ATTN_OK) return rc;
+    int J = 0;
+    const size_t need = gqa::prefill_split_plan(B, S, Hq, D, causal ? 1 : 0, sms, &J);
+    if (J > 0) {
+        void *ws = nullptr;
+        rc = workspace_acquire(need, st, true, &ws);
+        if (rc == ATTN_OK) {
+            const size_t blocks = need / ((size_t)256 * (D + 1) * sizeof(float));
+            a.J = J;
+            a.ws_o = static_cast<float *>(ws);
+            a.ws_lse = a.ws_o + blocks * 256 * D;
+        } else if (rc != ATTN_ERR_WORKSPACE) {
+            return rc;
+        }
+    }
+    return cuda_status(gqa::launch_prefill_tc(a, out_dtype == ATTN_F32, st));
+}
 
 }  // namespace
 
@@ -198,43 +271,29 @@ int attn_prefill_ex(const void *q, const void *k, const void *v, void *o, float 
             static_cast<const float *>(q), static_cast<const float *>(k),
             static_cast<const float *>(v), static_cast<float *>(o), lse, B, S, Hq, Hkv, D, scale,
             causal ? 1 : 0, st));
-    PrefillTcArgs a;
-    std::memset(&a, 0, sizeof(a));
-    if (!encode_bf16_rows(&a.tq, q, (long long)B * Hq, S) ||
-        !encode_bf16_rows(&a.tk, k, (long long)B * Hkv, S) ||
-        !encode_bf16_rows(&a.tv, v, (long long)B * Hkv, S))
-        return ATTN_ERR_CUDA;
-    a.o = o;
-    a.lse = lse;
-    a.B = B;
-    a.S = S;
-    a.Hq = Hq;
-    a.Hkv = Hkv;
-    a.scale_log2 = scale * 1.4426950408889634f;
-    a.causal = causal ? 1 : 0;
-    rc = status_ptr(&a.status);
+    return prefill_bf16(q, k, v, o, lse, B, S, Hq, Hkv, D, scale, causal, out_dtype,
+                        contiguous(Hq, S, D), contiguous(Hkv, S, D), contiguous(Hkv, S, D),
+                        contiguous(Hq, S, D), stream);
+}
+
+int attn_prefill_strided(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                         int S, int Hq, int Hkv, int D, const long long *q_strides,
+                         const long long *k_strides, const long long *v_strides,
+                         const long long *o_strides, float scale, int causal, int out_dtype,
+                         void *stream)
+{
+    if (!q_strides || !k_strides || !v_strides || !o_strides) return ATTN_ERR_INVALID;
+    int rc = check_prefill(q, k, v, o, lse, B, S, Hq, Hkv, D, scale, ATTN_BF16, out_dtype);
     if (rc != ATTN_OK) return rc;
-    // Small grids (fewer row blocks x heads than SMs) split the keys of each row block over
-    // several blocks and merge; the partials use the library-owned scratch. If that scratch
-    // cannot grow now (stream capture), the unsplit kernel runs instead.
-    int sms = 0;
-    rc = sm_count(&sms);
-    if (rc != ATTN_OK) return rc;
-    int J = 0;
-    const size_t need = gqa::prefill_split_plan(B, S, Hq, causal ? 1 : 0, sms, &J);
-    if (J > 0) {
-        void *ws = nullptr;
-        rc = workspace_acquire(need, st, true, &ws);
-        if (rc == ATTN_OK) {
-            const size_t blocks = need / ((size_t)256 * 129 * sizeof(float));
-            a.J = J;
-            a.ws_o = static_cast<float *>(ws);
-            a.ws_lse = a.ws_o + blocks * 256 * 128;
-        } else if (rc != ATTN_ERR_WORKSPACE) {
-            return rc;
-        }
-    }
-    return cuda_status(gqa::launch_prefill_tc(a, out_dtype == ATTN_F32, st));
+    const Strides qs{q_strides[0], q_strides[1], q_strides[2]};
+    const Strides ks{k_strides[0], k_strides[1], k_strides[2]};
+    const Strides vs{v_strides[0], v_strides[1], v_strides[2]};
+    const Strides os{o_strides[0], o_strides[1], o_strides[2]};
+    if (!strides_ok(qs, 2) || !strides_ok(ks, 2) || !strides_ok(vs, 2) ||
+        !strides_ok(os, out_dtype == ATTN_F32 ? 4 : 2))
+        return ATTN_ERR_ALIGN;
+    return prefill_bf16(q, k, v, o, lse, B, S, Hq, Hkv, D, scale, causal, out_dtype, qs, ks, vs,
+                        os, stream);
 }
 
 namespace {
@@ -275,16 +334,21 @@ int chunk_or_varlen(const void *q, const void *kcache, const void *vcache, const
     if ((long long)B * Hkv * max_len > (1LL << 40)) return ATTN_ERR_UNSUPPORTED;
     PrefillTcArgs a;
     std::memset(&a, 0, sizeof(a));
-    if (!encode_bf16_rows(&a.tq, q, (long long)B * Hq, Sq) ||
-        !encode_bf16_rows(&a.tk, kcache, (long long)B * Hkv, max_len) ||
-        !encode_bf16_rows(&a.tv, vcache, (long long)B * Hkv, max_len))
+    if (!encode_bf16_4d(&a.tq, q, D, Sq, Hq, B, contiguous(Hq, Sq, D)) ||
+        !encode_bf16_4d(&a.tk, kcache, D, max_len, Hkv, B, contiguous(Hkv, max_len, D)) ||
+        !encode_bf16_4d(&a.tv, vcache, D, max_len, Hkv, B, contiguous(Hkv, max_len, D)))
         return ATTN_ERR_CUDA;
+    const Strides os = contiguous(Hq, Sq, D);
     a.o = o;
+    a.o_sb = os.b;
+    a.o_ss = os.s;
+    a.o_sh = os.h;
     a.lse = lse;
     a.B = B;
     a.S = Sq;
     a.Hq = Hq;
     a.Hkv = Hkv;
+    a.D = D;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.causal = causal ? 1 : 0;
     a.kv_lens = seqlens;

@@ -8,18 +8,19 @@
 
 namespace gqa {
 
-// Prefill on tcgen05 tensor cores: bf16 q/k/v with head dim 128. The tensor maps describe
-// q [B*Hq, S, 128], k and v [B*Hkv, S, 128] as 3-D bf16 tensors with 64x128 boxes and
-// 128-byte swizzle.
+// Prefill on tcgen05 tensor cores: bf16 q/k/v with head dim 64 or 128. The tensor maps describe
+// q as a 4-D bf16 tensor {D, S, Hq, B} and k, v as {D, rows, Hkv, B} (rows = S, or max_kv for a
+// cache), each with its own strides, 64 x 128-row boxes and 128-byte swizzle.
 struct PrefillTcArgs {
     CUtensorMap tq, tk, tv;
-    void *o;        // [B, Hq, S, 128], bf16 or fp32
+    void *o;        // bf16 or fp32, element (b, h, i, d) at o + b o_sb + i o_ss + h o_sh + d
+    long long o_sb, o_ss, o_sh;
     float *lse;     // [B, Hq, S] or nullptr
-    int B, S, Hq, Hkv;
+    int B, S, Hq, Hkv, D;
     float scale_log2;  // scale * log2(e)
     int causal;
     unsigned *status;  // device status word
-    // chunk against a cache: k/v maps view [B*Hkv, max_kv rows]; kv_lens[b] keys per sequence
+    // chunk against a cache: k/v maps view max_kv rows per head; kv_lens[b] keys per sequence
     // (device); the S queries are the last S of them. nullptr: plain prefill (L = S).
     const int *kv_lens = nullptr;
     int max_kv = 0;
@@ -28,14 +29,13 @@ struct PrefillTcArgs {
     int front = 0;
     // key split for small grids (0 = none): blocks of at most J key tiles, partials in ws
     int J = 0;
-    float *ws_o = nullptr;    // [blocks, 256, 128] fp32
+    float *ws_o = nullptr;    // [blocks, 256, D] fp32
     float *ws_lse = nullptr;  // [blocks, 256] fp32
 };
 cudaError_t launch_prefill_tc(const PrefillTcArgs &a, bool out_f32, cudaStream_t stream);
 // Chooses the key split for a prefill shape on num_sms SMs: writes J (0 = no split) and returns
 // the workspace bytes it needs.
-size_t prefill_split_plan(int B, int S, int Hq, int causal, int num_sms, int *J);
-int prefill_tc_smem_bytes();
+size_t prefill_split_plan(int B, int S, int Hq, int D, int causal, int num_sms, int *J);
 
 // Prefill on CUDA cores in fp32 (fp32 q/k/v/o), head dim 64 or 128.
 cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, float *o,

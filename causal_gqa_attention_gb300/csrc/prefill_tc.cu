@@ -1,5 +1,7 @@
 // prefill_tc.cu -- fused attention forward (prefill) on sm_103a tensor cores, bf16 in,
-// fp32 accumulation and softmax state, head dim 128.
+// fp32 accumulation and softmax state, head dim 128 or 64. q, k, v are read through 4-D tensor
+// maps, so any layout with a contiguous head dim and 16-byte multiple strides works in place
+// (the [B, H, S, D] default, [B, S, H, D], or q/k/v as slices of one fused projection output).
 //
 // One thread block owns 256 consecutive query rows of one (batch, query head): two 128-row
 // Q tiles. Both tiles consume the same stream of 128-key K/V tiles, so every K/V tile brought
@@ -49,18 +51,26 @@ namespace {
 
 constexpr int BM = 128;        // query rows per tile = TMEM lanes
 constexpr int BN = 128;        // keys per K/V tile
-constexpr int HD = 128;        // head dim
 constexpr int kThreads = 384;  // 12 warps
 constexpr uint32_t kBox = 16384;          // one 128-row x 64-col bf16 box (128-byte rows)
-constexpr uint32_t kTile = 2 * kBox;      // 128 x 128 bf16
-constexpr uint32_t kOffQ = 0;             // 2 tiles
 constexpr int KST = 2;                    // K ring stages
 constexpr int VST = 3;                    // V ring stages (V also waits for its fp16 conversion)
-constexpr uint32_t kOffK = 2 * kTile;
-constexpr uint32_t kOffV = kOffK + KST * kTile;
-constexpr uint32_t kOffBar = kOffV + VST * kTile;
-constexpr uint32_t kSmem = kOffBar + 256 + 1024;  // + barriers, + alignment slack
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
+
+// Shared-memory plan for head dim HD (64 or 128): two Q tiles, the K ring, the V ring, then the
+// barriers. A tile is 128 rows x HD bf16, stored as HD / 64 boxes of 64 columns.
+template <int HD>
+struct Geo {
+    static_assert(HD == 64 || HD == 128, "head dim");
+    static constexpr int NBOX = HD / 64;
+    static constexpr uint32_t kTile = NBOX * kBox;
+    static constexpr uint32_t kOffQ = 0;
+    static constexpr uint32_t kOffK = 2 * kTile;
+    static constexpr uint32_t kOffV = kOffK + KST * kTile;
+    static constexpr uint32_t kOffBar = kOffV + VST * kTile;
+    static constexpr uint32_t kSmem = kOffBar + 256 + 1024;  // + barriers, + alignment slack
+    static_assert(kSmem <= 232448, "shared memory per block");
+};
 
 // TMEM column bases
 constexpr uint32_t kColS = 0;    // + 128 t
@@ -81,7 +91,6 @@ enum : int {
     NUM_BARS = B_DRAIN + 1
 };
 static_assert(NUM_BARS * 8 + 8 <= 256, "barrier area");
-static_assert(kSmem <= 232448, "shared memory per block");
 
 __host__ __device__ __forceinline__ int last_key_tile(int causal, int q_first, int nkv)
 {
@@ -118,28 +127,35 @@ __device__ __forceinline__ uint32_t too_big_for_f16(uint32_t w)
     return (uint32_t)((w & 0x7FFF0000u) >= 0x47800000u) | (uint32_t)((w & 0x7FFFu) >= 0x4780u);
 }
 
-// Zeroes rows >= rows_ok of a 128 x 128 bf16 tile: the 16-byte chunks ct, ct + 64, ... only.
+// Zeroes rows >= rows_ok of a 128-row bf16 tile of nchunk 16-byte chunks (64-column boxes of
+// 1024 chunks, 8 per row): the chunks ct, ct + 64, ... only.
 // Out of line on purpose: inlined (or folded into the conversion loop as a per-chunk select) it
 // cost the whole kernel 2-12% on full-length prefill, where it never runs.
-__device__ __noinline__ void zero_v_tail(uint4 *tile, int ct, int rows_ok)
+__device__ __noinline__ void zero_v_tail(uint4 *tile, int ct, int rows_ok, int nchunk)
 {
-    for (int c = ct; c < (int)(kTile / 16); c += 64)
+    for (int c = ct; c < nchunk; c += 64)
         if (((c & 1023) >> 3) >= rows_ok) tile[c] = make_uint4(0, 0, 0, 0);
 }
 
+// HD: head dim (64 or 128). The tensor maps are 4-D {HD, rows, heads, batch} with any strides,
+// so q, k and v may be views (a [B, S, H, D] layout, a fused QKV projection output); O is
+// written at out + b o_sb + i o_ss + h o_sh (elements), the LSE as [B, Hq, S].
 // SPLIT = false: one block per (row block, head, batch), final O and LSE.
 // SPLIT = true: one block per (row block, key segment of J tiles, head, batch); it writes the
 // segment's normalised O (fp32) and its LSE (log2 units) to ws_o / ws_lse, and
 // prefill_split_merge_kernel combines the segments of each row.
-template <bool OUT_F32, bool SPLIT>
+template <int HD, bool OUT_F32, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, void *__restrict__ out,
                       float *__restrict__ lse, int B, int S, int Hq, int Hkv, float scale_log2,
                       int causal, unsigned *__restrict__ status, int J, float *__restrict__ ws_o,
                       float *__restrict__ ws_lse, const int *__restrict__ kv_lens, int max_kv,
-                      int front)
+                      int front, long long o_sb, long long o_ss, long long o_sh)
 {
+    using G = Geo<HD>;
+    constexpr uint32_t kTile = G::kTile, kOffQ = G::kOffQ, kOffK = G::kOffK, kOffV = G::kOffV,
+                       kOffBar = G::kOffBar;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -233,28 +249,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tq);
             tma_prefetch_desc(&tk);
             tma_prefetch_desc(&tv);
-            const int zq = b * Hq + h, zk = b * Hkv + g;
             mbar_arrive_expect_tx(&bar[B_Q], n_tiles * kTile);
             for (int t = 0; t < n_tiles; ++t)
-                for (int x = 0; x < 2; ++x)
-                    tma_load_3d(smem + kOffQ + t * kTile + x * kBox, &tq, &bar[B_Q], x * 64,
-                                q0 + t * BM, zq);
+                for (int x = 0; x < G::NBOX; ++x)
+                    tma_load_4d(smem + kOffQ + t * kTile + x * kBox, &tq, &bar[B_Q], x * 64,
+                                q0 + t * BM, h, b);
             int issued_k[KST] = {}, issued_v[VST] = {};
             for (int jj = 0; jj < nJ; ++jj) {
                 const int j = jb + jj;
                 const int sk = jj % KST, uk = jj / KST;
                 if (uk > 0 && !mbar_wait(&bar[B_KEMPTY + sk], (uk - 1) & 1, abort_flag)) break;
                 mbar_arrive_expect_tx(&bar[B_KFULL + sk], kTile);
-                for (int x = 0; x < 2; ++x)
-                    tma_load_3d(smem + kOffK + sk * kTile + x * kBox, &tk, &bar[B_KFULL + sk],
-                                x * 64, j * BN, zk);
+                for (int x = 0; x < G::NBOX; ++x)
+                    tma_load_4d(smem + kOffK + sk * kTile + x * kBox, &tk, &bar[B_KFULL + sk],
+                                x * 64, j * BN, g, b);
                 issued_k[sk] = uk + 1;
                 const int sv = jj % VST, uv = jj / VST;
                 if (uv > 0 && !mbar_wait(&bar[B_VEMPTY + sv], (uv - 1) & 1, abort_flag)) break;
                 mbar_arrive_expect_tx(&bar[B_VFULL + sv], kTile);
-                for (int x = 0; x < 2; ++x)
-                    tma_load_3d(smem + kOffV + sv * kTile + x * kBox, &tv, &bar[B_VFULL + sv],
-                                x * 64, j * BN, zk);
+                for (int x = 0; x < G::NBOX; ++x)
+                    tma_load_4d(smem + kOffV + sv * kTile + x * kBox, &tv, &bar[B_VFULL + sv],
+                                x * 64, j * BN, g, b);
                 issued_v[sv] = uv + 1;
             }
             if (*abort_flag) {
@@ -295,8 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t vbase = sV + ((jj - 1) % VST) * kTile;
 #pragma unroll
                         for (int kk = 0; kk < BN / 16; ++kk) {
-                            // B = V rows 16kk..16kk+15: MN-major, 64-col chunks 16 KB apart,
-                            // 8-row groups 1 KB apart
+                            // B = V rows 16kk..16kk+15: MN-major, 64-col chunks 16 KB apart
+                            // (one chunk when HD = 64), 8-row groups 1 KB apart
                             const uint64_t bd = smem_desc_sw128(vbase + kk * 2048, kBox, 1024);
                             mma_ts(tmem + kColO + t * 128, tmem + kColS + t * 128 + kk * 8, bd,
                                    idO, (jj - 1 > 0 || kk > 0) ? 1u : 0u);
@@ -340,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // 0 there, but 0 * NaN would not be. Each thread zeroes only the chunks it converts
             // below, so program order is the only ordering needed.
             const int rows_ok = L - (jb + jj) * BN;  // >= BN except on the tile holding L
-            if (rows_ok < BN) zero_v_tail(tile, ct, rows_ok);
+            if (rows_ok < BN) zero_v_tail(tile, ct, rows_ok, (int)(kTile / 16));
 #pragma unroll 4
             for (int c = ct; c < (int)(kTile / 16); c += 64) {
                 uint4 w = tile[c];
@@ -424,11 +439,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 l = fmaf(l, alpha, (rsa.x + rsa.y) + (rsb.x + rsb.y));
                 if (jj > 0 && __any_sync(0xffffffffu, need)) {
-                    uint32_t ov[128];
-                    tmem_ld128(tO, ov);
+                    uint32_t ov[HD];
+                    if constexpr (HD == 128) {
+                        tmem_ld128(tO, ov);
+                    } else {
+                        tmem_ld32(tO, ov);
+                        tmem_ld32(tO + 32, ov + 32);
+                    }
                     const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-                    for (int e = 0; e < 64; ++e) {
+                    for (int e = 0; e < HD / 2; ++e) {
                         const float2 v2 = fmul2(make_float2(__uint_as_float(ov[2 * e]),
                                                             __uint_as_float(ov[2 * e + 1])),
                                                 a2);
@@ -436,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ov[2 * e + 1] = __float_as_uint(v2.y);
                     }
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) tmem_st32(tO + c * 32, &ov[c * 32]);
+                    for (int c = 0; c < HD / 32; ++c) tmem_st32(tO + c * 32, &ov[c * 32]);
                 }
                 tmem_st_wait();
                 tc_fence_before();
@@ -454,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float inv = (active && l > 0.f) ? 1.f / l : 0.f;
                 const size_t prow = (size_t)blockIdx.x * (2 * BM) + t * BM + r;
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < HD / 32; ++c) {
                     uint32_t ov[32];
                     if (active) tmem_ld32(tO + c * 32, ov);
                     if (!live) continue;
@@ -474,8 +494,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool live = i < S;
                 const float inv = (active && l > 0.f) ? 1.f / l : 0.f;
                 const size_t orow = ((size_t)b * Hq + h) * S + (live ? i : 0);
+                const long long obase = b * o_sb + h * o_sh + (long long)(live ? i : 0) * o_ss;
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < HD / 32; ++c) {
                     uint32_t ov[32];
                     if (active)
                         tmem_ld32(tO + c * 32, ov);
@@ -485,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!live) continue;
                     if (OUT_F32) {
                         float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(out) +
-                                                                 orow * HD + c * 32);
+                                                                 obase + c * 32);
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
                             dst[e] = make_float4(__uint_as_float(ov[4 * e]) * inv,
@@ -494,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                  __uint_as_float(ov[4 * e + 3]) * inv);
                     } else {
                         uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(out) +
-                                                               orow * HD + c * 32);
+                                                               obase + c * 32);
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             uint32_t w[4];
@@ -523,14 +544,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (SPLIT) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Combine the key segments of each query row (split mode): one warp per row, four dims per
-// lane; segment weights 2^(lse_s - M), M = max_s lse_s, in segment order.
-template <bool OUT_F32>
+// Combine the key segments of each query row (split mode): one warp per row, HD / 32 dims per
+// lane; segment weights 2^(lse_s - M), M = max_s lse_s, in segment order. O is written with the
+// strides of the kernel above, the LSE as [B, Hq, S].
+template <int HD, bool OUT_F32>
 __global__ void __launch_bounds__(256)
     prefill_split_merge_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_lse,
                                void *__restrict__ out, float *__restrict__ lse, int B, int S,
-                               int Hq, int causal, int J)
+                               int Hq, int causal, int J, long long o_sb, long long o_ss,
+                               long long o_sh)
 {
+    constexpr int DPL = HD / 32;  // dims per lane: 4 or 2
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const long long row = (long long)blockIdx.x * 8 + warp;
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -542,7 +566,7 @@ __global__ void __launch_bounds__(256)
     int first = 0;  // first block of row block rb
     for (int r2 = n_rb - 1; r2 > rb; --r2) first += rb_segments(r2, S, causal, J) * Hq * B;
     const int nseg = rb_segments(rb, S, causal, J);
-    // every load of the row in one round: segment LSEs and this lane's four dims of each O
+    // every load of the row in one round: segment LSEs and this lane's dims of each O
     float ls[8];
     float4 x[8];
 #pragma unroll
@@ -552,8 +576,13 @@ __global__ void __launch_bounds__(256)
         if (k < nseg) {
             const size_t item = (size_t)first + (size_t)k * Hq * B + hb;
             ls[k] = ws_lse[item * (2 * BM) + rloc];
-            x[k] = *reinterpret_cast<const float4 *>(ws_o + (item * (2 * BM) + rloc) * HD +
-                                                     lane * 4);
+            const float *src = ws_o + (item * (2 * BM) + rloc) * HD + lane * DPL;
+            if constexpr (DPL == 4) {
+                x[k] = *reinterpret_cast<const float4 *>(src);
+            } else {
+                const float2 y = *reinterpret_cast<const float2 *>(src);
+                x[k] = make_float4(y.x, y.y, 0.f, 0.f);
+            }
         }
     }
     float M = ls[0];
@@ -573,20 +602,31 @@ __global__ void __launch_bounds__(256)
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     const size_t orow = (size_t)row;
+    const int b = hb / Hq, h = hb % Hq;
+    const long long obase = b * o_sb + h * o_sh + (long long)i * o_ss + lane * DPL;
     if (OUT_F32) {
-        *reinterpret_cast<float4 *>(static_cast<float *>(out) + orow * HD + lane * 4) =
-            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        float *dst = static_cast<float *>(out) + obase;
+        if constexpr (DPL == 4)
+            *reinterpret_cast<float4 *>(dst) =
+                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        else
+            *reinterpret_cast<float2 *>(dst) = make_float2(acc.x * inv, acc.y * inv);
     } else {
-        uint2 w2;
-        w2.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-        w2.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-        *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(out) + orow * HD + lane * 4) = w2;
+        __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(out) + obase;
+        if constexpr (DPL == 4) {
+            uint2 w2;
+            w2.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+            w2.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+            *reinterpret_cast<uint2 *>(dst) = w2;
+        } else {
+            *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(acc.x * inv, acc.y * inv);
+        }
     }
     if (lse != nullptr && lane == 0)
         lse[orow] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
 }
 
-template <bool OUT_F32, bool SPLIT>
+template <int HD, bool OUT_F32, bool SPLIT>
 cudaError_t launch_t(const PrefillTcArgs &a, cudaStream_t st)
 {
     static bool attr_set[64] = {};  // the attribute is set once per device
@@ -594,8 +634,8 @@ cudaError_t launch_t(const PrefillTcArgs &a, cudaStream_t st)
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 64 || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(prefill_tc_kernel<OUT_F32, SPLIT>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        e = cudaFuncSetAttribute(prefill_tc_kernel<HD, OUT_F32, SPLIT>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<HD>::kSmem);
         if (e != cudaSuccess) return e;
         if (dev < 64) attr_set[dev] = true;
     }
@@ -605,9 +645,10 @@ cudaError_t launch_t(const PrefillTcArgs &a, cudaStream_t st)
         blocks = 0;
         for (int rb = 0; rb < n_rb; ++rb) blocks += (long long)rb_segments(rb, a.S, a.causal, a.J) * a.Hq * a.B;
     }
-    prefill_tc_kernel<OUT_F32, SPLIT><<<(unsigned)blocks, kThreads, kSmem, st>>>(
+    prefill_tc_kernel<HD, OUT_F32, SPLIT><<<(unsigned)blocks, kThreads, Geo<HD>::kSmem, st>>>(
         a.tq, a.tk, a.tv, a.o, a.lse, a.B, a.S, a.Hq, a.Hkv, a.scale_log2, a.causal, a.status,
-        a.J, a.ws_o, a.ws_lse, a.kv_lens, a.kv_lens ? a.max_kv : a.S, a.front);
+        a.J, a.ws_o, a.ws_lse, a.kv_lens, a.kv_lens ? a.max_kv : a.S, a.front, a.o_sb, a.o_ss,
+        a.o_sh);
     e = cudaGetLastError();
     if (e != cudaSuccess || !SPLIT) return e;
     const long long rows = (long long)a.B * a.Hq * a.S;
@@ -620,21 +661,29 @@ cudaError_t launch_t(const PrefillTcArgs &a, cudaStream_t st)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_split_merge_kernel<OUT_F32>, (const float *)a.ws_o,
-                              (const float *)a.ws_lse, a.o, a.lse, a.B, a.S, a.Hq, a.causal, a.J);
+    return cudaLaunchKernelEx(&cfg, prefill_split_merge_kernel<HD, OUT_F32>, (const float *)a.ws_o,
+                              (const float *)a.ws_lse, a.o, a.lse, a.B, a.S, a.Hq, a.causal, a.J,
+                              a.o_sb, a.o_ss, a.o_sh);
+}
+
+template <int HD>
+cudaError_t launch_hd(const PrefillTcArgs &a, bool out_f32, cudaStream_t st)
+{
+    if (a.J > 0)
+        return out_f32 ? launch_t<HD, true, true>(a, st) : launch_t<HD, false, true>(a, st);
+    return out_f32 ? launch_t<HD, true, false>(a, st) : launch_t<HD, false, false>(a, st);
 }
 
 }  // namespace
 
-int prefill_tc_smem_bytes() { return (int)kSmem; }
-
 cudaError_t launch_prefill_tc(const PrefillTcArgs &a, bool out_f32, cudaStream_t st)
 {
-    if (a.J > 0) return out_f32 ? launch_t<true, true>(a, st) : launch_t<false, true>(a, st);
-    return out_f32 ? launch_t<true, false>(a, st) : launch_t<false, false>(a, st);
+    if (a.D == 64) return launch_hd<64>(a, out_f32, st);
+    if (a.D == 128) return launch_hd<128>(a, out_f32, st);
+    return cudaErrorInvalidValue;
 }
 
-size_t prefill_split_plan(int B, int S, int Hq, int causal, int num_sms, int *J_out)
+size_t prefill_split_plan(int B, int S, int Hq, int D, int causal, int num_sms, int *J_out)
 {
     // Split the key range only when the plain grid leaves SMs idle: pick the longest segment
     // (fewest blocks) whose grid still fits in one wave; at most 8 segments per row block.
@@ -661,7 +710,7 @@ size_t prefill_split_plan(int B, int S, int Hq, int causal, int num_sms, int *J_
     *J_out = best;
     long long blocks = 0;
     for (int rb = 0; rb < n_rb; ++rb) blocks += (long long)rb_segments(rb, S, causal, best) * Hq * B;
-    return (size_t)blocks * (2 * BM) * (HD + 1) * sizeof(float);
+    return (size_t)blocks * (2 * BM) * (D + 1) * sizeof(float);
 }
 
 }  // namespace gqa

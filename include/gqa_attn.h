@@ -71,7 +71,7 @@ typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype;
  *   o   [B, Hq,  S, D] bf16        lse  [B, Hq, S] fp32, natural log; may be NULL
  *   scale multiplies the scores before the softmax (usually 1/sqrt(D)).
  *   causal != 0: query i sees keys 0..i.
- * Requires Hq % Hkv == 0, D == 128, 16-byte aligned pointers.
+ * Requires Hq % Hkv == 0, D in {64, 128}, 16-byte aligned pointers.
  * When the shape has fewer (256-row block, head) tiles than the GPU has SMs, the key range of
  * each row block is split over several thread blocks and a second kernel merges their results
  * by log-sum-exp weights; the partial results use the library-owned scratch buffer (grown with
@@ -85,7 +85,7 @@ int attn_prefill(const void *q, const void *k, const void *v, void *o, float *ls
 
 /*
  * attn_prefill_ex -- prefill with explicit element types.
- *   in_dtype  ATTN_BF16: q, k, v bf16; D == 128; tensor-core kernel (as attn_prefill).
+ *   in_dtype  ATTN_BF16: q, k, v bf16; D in {64, 128}; tensor-core kernel (as attn_prefill).
  *             ATTN_F32:  q, k, v fp32; D in {64, 128}; fp32 CUDA-core kernel (fp32 products,
  *                        sums and exponentials throughout).
  *   out_dtype ATTN_BF16 or ATTN_F32 for o (ATTN_F32 with bf16 inputs returns the fp32 result
@@ -95,6 +95,32 @@ int attn_prefill(const void *q, const void *k, const void *v, void *o, float *ls
 int attn_prefill_ex(const void *q, const void *k, const void *v, void *o, float *lse, int B,
                     int S, int Hq, int Hkv, int D, float scale, int causal, int in_dtype,
                     int out_dtype, void *stream);
+
+/*
+ * attn_prefill_strided -- attn_prefill for bf16 operands in any layout whose head dim is
+ * contiguous: each of q, k, v, o is described by its base pointer and three element strides
+ * {batch, token, head}. Element (b, h, i, d) of q is q[b*qs[0] + i*qs[1] + h*qs[2] + d]; k, v and
+ * o likewise with their own strides. Examples: [B, H, S, D] contiguous is {H*S*D, D, S*D};
+ * [B, S, H, D] contiguous is {S*H*D, H*D, D}; the output of a fused QKV projection
+ * [B, S, Hq + 2*Hkv, D] gives q = base, k = base + Hq*D, v = base + (Hq + Hkv)*D, all with the
+ * strides {S*(Hq+2*Hkv)*D, (Hq+2*Hkv)*D, D}. The operands are read in place (no copy).
+ *   q_strides, k_strides, v_strides, o_strides: host arrays of 3 int64, each > 0 and a multiple
+ *   of 16 bytes (8 bf16 elements; 4 for an fp32 o), else ATTN_ERR_ALIGN; NULL: ATTN_ERR_INVALID.
+ *   o bf16 or fp32 by out_dtype; lse [B, Hq, S] fp32 contiguous, or NULL.
+ * Other arguments, requirements and numerics as attn_prefill (D in {64, 128}). Overlapping o
+ * elements (strides that alias) are the caller's error.
+ * Sources: "Attention three-op fusion" (xdnf.cn/news/349386) section 6.1, second item (after the
+ * projection weights are merged Q, K and V sit in one contiguous buffer; the kernel's address
+ * arithmetic follows that layout instead of three separate tensors); "Hand-written Triton
+ * decoder" (m.nlpx.cn/news/28229) section 2.2, operations 2, 3 and 9 (one projection writes
+ * q, k and v side by side; splitting q into heads and merging the heads' outputs back into the
+ * hidden layout are stride changes, not kernels).
+ */
+int attn_prefill_strided(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                         int S, int Hq, int Hkv, int D, const long long *q_strides,
+                         const long long *k_strides, const long long *v_strides,
+                         const long long *o_strides, float scale, int causal, int out_dtype,
+                         void *stream);
 
 /*
  * attn_chunk -- a chunk of Sq new query tokens per sequence against a bf16 KV cache (chunked
@@ -108,7 +134,7 @@ int attn_prefill_ex(const void *q, const void *k, const void *v, void *o, float 
  *   seqlens  [B] int32, device memory; values outside [0, max_len] are clamped and flagged
  *            (ATTN_DEV_SEQLEN_CLAMPED)
  *   o        [B, Hq, Sq, D], bf16 or fp32 by out_dtype; lse [B, Hq, Sq] fp32 or NULL
- * Requires Hq % Hkv == 0, D == 128. Same tensor-core kernel as attn_prefill (with
+ * Requires Hq % Hkv == 0, D in {64, 128}. Same tensor-core kernel as attn_prefill (with
  * seqlens[b] = Sq = S, max_len = S it computes exactly attn_prefill's result).
  * Sources: "Hand-written Triton decoder" (m.nlpx.cn/news/28229) section 1.4 (speculative
  * decoding and beam search reuse the attention kernels with several new tokens);
@@ -125,7 +151,7 @@ int attn_chunk(const void *q, const void *kcache, const void *vcache, const int 
  * (i >= seqlens[b]) get o = 0 and lse = -inf.
  *   q [B, Hq, S, D] bf16, k/v [B, Hkv, S, D] bf16, seqlens [B] int32 (device, clamped to
  *   [0, S] and flagged with ATTN_DEV_SEQLEN_CLAMPED), o [B, Hq, S, D] bf16 or fp32 by
- *   out_dtype, lse [B, Hq, S] fp32 or NULL. Requires Hq % Hkv == 0, D == 128.
+ *   out_dtype, lse [B, Hq, S] fp32 or NULL. Requires Hq % Hkv == 0, D in {64, 128}.
  * Source: "Attention three-op fusion" (xdnf.cn/news/349386) section 4.3 (padding mask: positions
  * at or past the sequence length get score -infinity) and section 6.1 (dynamic shapes).
  */

@@ -69,7 +69,8 @@ def check_lse(lse_gpu, lse_ref, what: str):
     l = to64(lse_gpu)
     assert l.shape == lse_ref.shape
     both_ninf = np.isneginf(l) & np.isneginf(lse_ref)
-    err = np.where(both_ninf, 0.0, np.abs(l - lse_ref))
+    with np.errstate(invalid="ignore"):  # -inf - -inf where both are empty rows
+        err = np.where(both_ninf, 0.0, np.abs(l - lse_ref))
     assert np.isfinite(err).all(), f"{what}: non-finite lse error"
     assert err.max() <= TOL_LSE, f"{what}: lse max err {err.max():.3e}"
     return float(err.max())

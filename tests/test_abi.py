@@ -65,7 +65,8 @@ A16 = 1 << 20  # a 16-byte aligned fake device address; never dereferenced (reje
     ((A16, A16, A16, A16, None, 1, 8, 2, 1, 128, 0.0, 1, 1, 1), 1),  # scale 0
     ((A16, A16, A16, A16, None, 1, 8, 2, 1, 128, float("nan"), 1, 1, 1), 1),
     ((A16, A16, A16, A16, None, 1, 8, 2, 1, 128, 0.1, 1, 7, 1), 1),  # bad dtype
-    ((A16, A16, A16, A16, None, 1, 8, 2, 1, 64, 0.1, 1, 1, 1), 2),   # bf16 needs D = 128
+    ((A16, A16, A16, A16, None, 1, 8, 2, 1, 96, 0.1, 1, 1, 1), 2),   # bf16 needs D in {64, 128}
+    ((A16, A16, A16, A16, None, 1, 8, 2, 1, 32, 0.1, 1, 1, 1), 2),
     ((A16, A16, A16, A16, None, 1, 8, 2, 1, 96, 0.1, 1, 0, 0), 2),   # fp32 D = 96
     ((A16, A16, A16, A16, None, 1, 8, 2, 1, 64, 0.1, 1, 0, 1), 2),   # fp32 in, bf16 out
     ((A16 + 8, A16, A16, A16, None, 1, 8, 2, 1, 128, 0.1, 1, 1, 1), 3),  # misaligned q
@@ -73,6 +74,35 @@ A16 = 1 << 20  # a 16-byte aligned fake device address; never dereferenced (reje
 ])
 def test_prefill_rejects_on_host(lib, args, code):
     assert lib.attn_prefill_ex(*args, None) == code
+
+
+def _ll3(a, b, c):
+    return (ctypes.c_longlong * 3)(a, b, c)
+
+
+# every case is rejected before any CUDA call (the pointers are never dereferenced)
+@pytest.mark.parametrize("strides,code", [
+    ((None, (8, 8, 8), (8, 8, 8), (8, 8, 8)), 1),                     # NULL stride array
+    (((1024, 132, 8), (8, 8, 8), (8, 8, 8), (8, 8, 8)), 3),           # q token stride 264 B
+    (((1024, 128, 8), (8, 8, 4), (8, 8, 8), (8, 8, 8)), 3),           # k head stride 8 B
+    (((1024, 128, 8), (8, 8, 8), (0, 8, 8), (8, 8, 8)), 3),           # v batch stride 0
+    (((1024, 128, 8), (8, 8, 8), (8, 8, 8), (8, 8, -8)), 3),          # negative o stride
+    (((1024, 128, 8), (8, 8, 8), (8, 8, 8), (8, 1 << 40, 8)), 3),     # huge o stride
+])
+def test_prefill_strided_rejects_on_host(lib, strides, code):
+    arrs = [None if st is None else _ll3(*st) for st in strides]
+    assert lib.attn_prefill_strided(A16, A16, A16, A16, None, 1, 8, 2, 1, 64, *arrs, 0.1, 1, 1,
+                                    None) == code
+
+
+def test_prefill_strided_fp32_out_stride(lib):
+    # an o token stride of 6 fp32 elements (24 B) is not a 16-byte multiple
+    ok = _ll3(1024, 128, 8)
+    assert lib.attn_prefill_strided(A16, A16, A16, A16, None, 1, 8, 2, 1, 64, ok, ok, ok,
+                                    _ll3(1024, 6, 8), 0.1, 1, 0, None) == 3
+    # unsupported head dim before strides are looked at
+    assert lib.attn_prefill_strided(A16, A16, A16, A16, None, 1, 8, 2, 1, 96, ok, ok, ok, ok,
+                                    0.1, 1, 1, None) == 2
 
 
 @pytest.mark.parametrize("args,code", [
