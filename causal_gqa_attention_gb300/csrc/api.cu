@@ -436,22 +436,31 @@ int attn_decode_rope(const void *q, const void *k_new, const void *v_new, const 
                           out_dtype);
     if (rc != ATTN_OK) return rc;
     if (!k_new || !v_new || !cos_t || !sin_t) return ATTN_ERR_INVALID;
-    if (!aligned4(cos_t) || !aligned4(sin_t) || (reinterpret_cast<uintptr_t>(k_new) & 1u) ||
-        (reinterpret_cast<uintptr_t>(v_new) & 1u))
+    if (!aligned16(cos_t) || !aligned16(sin_t) || !aligned16(k_new) || !aligned16(v_new))
         return ATTN_ERR_ALIGN;
+    const bool fused = gqa::decode_fuses_rope(B);
     const size_t dec = (gqa::decode_workspace_bytes(B, Hq, Hkv, D, max_len) + 255) & ~(size_t)255;
-    const size_t need = dec + (size_t)B * Hq * D * sizeof(float);
+    const size_t need = dec + (fused ? 0 : (size_t)B * Hq * D * sizeof(float));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     void *ws = nullptr;
     rc = workspace_acquire(need, st, true, &ws);
     if (rc != ATTN_OK) return rc;
-    float *q_rot = reinterpret_cast<float *>(static_cast<char *>(ws) + dec);
-    rc = cuda_status(gqa::launch_rope_append(q, k_new, v_new, cos_t, sin_t, kcache, vcache,
-                                             seqlens, q_rot, B, Hq, Hkv, D, max_len, st));
-    if (rc != ATTN_OK) return rc;
     DecodeArgs a;
-    a.q = q_rot;
-    a.q_f32 = true;
+    if (fused) {
+        // one kernel: RoPE of q and of the new key, cache store, attention
+        a.q = q;
+        a.k_new = k_new;
+        a.v_new = v_new;
+        a.cos_t = cos_t;
+        a.sin_t = sin_t;
+    } else {
+        float *q_rot = reinterpret_cast<float *>(static_cast<char *>(ws) + dec);
+        rc = cuda_status(gqa::launch_rope_append(q, k_new, v_new, cos_t, sin_t, kcache, vcache,
+                                                 seqlens, q_rot, B, Hq, Hkv, D, max_len, st));
+        if (rc != ATTN_OK) return rc;
+        a.q = q_rot;
+        a.q_f32 = true;
+    }
     a.kc = kcache;
     a.vc = vcache;
     a.seqlens = seqlens;

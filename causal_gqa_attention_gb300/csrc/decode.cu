@@ -212,6 +212,77 @@ __device__ __forceinline__ void load_q(const QT *q, size_t row0, int gl, float s
     }
 }
 
+// RoPE for decode (rotate-half): the pair (d, d + D/2) becomes
+// [x1 cos - x2 sin, x1 sin + x2 cos] with the angle tables' row of the token's position. Lane gl
+// of a key group holds dims gl*8 .. gl*8+7; the partner half sits LPK/2 lanes away, so one
+// exchange gives every lane both halves of its 8 pairs. cs / sn point at the tables' row.
+// The table entries this lane needs: pairs (gl % HALF) * 8 .. + 7 of the row.
+template <int D>
+__device__ __forceinline__ void rope_angles(int gl, const float *cs, const float *sn,
+                                            float (&c)[8], float (&sv)[8])
+{
+    constexpr int HALF = D / 16;  // LPK / 2
+    const int i0 = (gl % HALF) * 8;
+    const float4 c0 = *reinterpret_cast<const float4 *>(cs + i0);
+    const float4 c1 = *reinterpret_cast<const float4 *>(cs + i0 + 4);
+    const float4 s0 = *reinterpret_cast<const float4 *>(sn + i0);
+    const float4 s1 = *reinterpret_cast<const float4 *>(sn + i0 + 4);
+    c[0] = c0.x; c[1] = c0.y; c[2] = c0.z; c[3] = c0.w;
+    c[4] = c1.x; c[5] = c1.y; c[6] = c1.z; c[7] = c1.w;
+    sv[0] = s0.x; sv[1] = s0.y; sv[2] = s0.z; sv[3] = s0.w;
+    sv[4] = s1.x; sv[5] = s1.y; sv[6] = s1.z; sv[7] = s1.w;
+}
+
+template <int D>
+__device__ __forceinline__ void rope_rotate8(float (&x)[8], int gl, const float (&c)[8],
+                                             const float (&sv)[8])
+{
+    constexpr int HALF = D / 16;
+    const bool upper = gl >= HALF;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const float other = __shfl_xor_sync(0xffffffffu, x[e], HALF);
+        x[e] = upper ? other * sv[e] + x[e] * c[e] : x[e] * c[e] - other * sv[e];
+    }
+}
+
+// Eight bf16 values of one row, widened to fp32.
+__device__ __forceinline__ void load_bf16x8(const __nv_bfloat16 *src, float (&x)[8])
+{
+    const uint4 w = *reinterpret_cast<const uint4 *>(src);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        x[2 * e] = bf16lo(ws[e]);
+        x[2 * e + 1] = bf16hi(ws[e]);
+    }
+}
+
+// q fragment as load_q, rotated by RoPE first (in fp32, never rounded).
+template <int D, int HG>
+__device__ __forceinline__ void load_q_rope(const __nv_bfloat16 *q, size_t row0, int gl,
+                                            float scale_log2, const float (&c)[8],
+                                            const float (&sv)[8], float2 (&qp)[HG][4])
+{
+#pragma unroll
+    for (int h = 0; h < HG; ++h) {
+        float x[8];
+        load_bf16x8(q + (row0 + h) * D + gl * 8, x);
+        rope_rotate8<D>(x, gl, c, sv);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            qp[h][e] = make_float2(x[2 * e] * scale_log2, x[2 * e + 1] * scale_log2);
+    }
+}
+
+// The new token's K/V for decode with RoPE (unrotated key, value, angle tables, and the cache
+// to store the rotated key and the value in). Unused (null) in plain decode.
+struct RopeIn {
+    const __nv_bfloat16 *k_new, *v_new;  // [B, Hkv, D]
+    const float *cos_t, *sin_t;          // [max_len, D/2]
+    __nv_bfloat16 *kc, *vc;              // the caches, written at row seqlens[b] - 1
+};
+
 template <int D, int HG, typename QT>
 __global__ void __launch_bounds__(kWarps * 32)
     decode_split_kernel(const QT *__restrict__ q, const __nv_bfloat16 *__restrict__ kc,
@@ -416,12 +487,18 @@ __device__ __forceinline__ void cursor_advance(StreamCursor &c, int n, const int
     }
 }
 
-template <int D, int HG, typename QT>
+// ROPE: the step also applies RoPE to q and to the new key at position seqlens[b] - 1 and
+// stores the new key and value in the cache. The warp whose stage holds that row (the last key
+// of a stream) replaces the row in shared memory (it was loaded before the store) with the
+// rotated key, rounded to bf16 as the cache holds it, and the value; the stream of query-head
+// subgroup 0 of each kv head also writes them to the cache.
+template <int D, int HG, bool ROPE>
 __global__ void __launch_bounds__(kWarps * 32)
-    decode_stream_kernel(const QT *__restrict__ q, const __nv_bfloat16 *__restrict__ kc,
+    decode_stream_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ kc,
                          const __nv_bfloat16 *__restrict__ vc, const int *__restrict__ seqlens,
                          float *__restrict__ ws_o, float2 *__restrict__ ws_ml, int B, int Hq,
-                         int Hkv, int max_len, float scale_log2, unsigned *__restrict__ status)
+                         int Hkv, int max_len, float scale_log2, unsigned *__restrict__ status,
+                         RopeIn rope)
 {
     using P = Plan<D, HG>;
     constexpr int LPK = P::LPK, GPW = P::GPW, T = P::T, NV = P::NV, SK = P::SK;
@@ -518,6 +595,7 @@ __global__ void __launch_bounds__(kWarps * 32)
         float m_ref[HG];
         float2 acc[HG][4];
         float l_own[NV];
+        uint4 new_k = make_uint4(0, 0, 0, 0), new_v = new_k;  // RoPE: the new row, packed bf16
         float2 *pw = pbuf + (warp * GPW + grp) * T * HG;
         volatile int never = 0;
         int it = 0;
@@ -528,7 +606,28 @@ __global__ void __launch_bounds__(kWarps * 32)
             const bool last = (cc.off + n == cc.Lb) || (cc.pos + n == r1);
             if (first) {
                 const int g = cc.sl / SUB, gs = cc.sl % SUB;
-                load_q<D, HG, QT>(q, (size_t)cc.b * Hq + g * G + gs * HG, gl, scale_log2, qp);
+                if constexpr (ROPE) {
+                    // angles of the newest token's position, for q and (when this slice ends
+                    // the stream) for the new key, which is rotated and packed here so the
+                    // stage that holds its row needs no global load
+                    const size_t prow = (size_t)(cc.Lb - 1) * (D / 2);
+                    float c[8], sv[8];
+                    rope_angles<D>(gl, rope.cos_t + prow, rope.sin_t + prow, c, sv);
+                    load_q_rope<D, HG>(q, (size_t)cc.b * Hq + g * G + gs * HG, gl, scale_log2,
+                                       c, sv, qp);
+                    if (cc.pos + (cc.Lb - cc.off) <= r1) {
+                        const size_t src = ((size_t)cc.b * Hkv + g) * D + gl * 8;
+                        float x[8];
+                        load_bf16x8(rope.k_new + src, x);
+                        rope_rotate8<D>(x, gl, c, sv);
+                        new_k = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]),
+                                           pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
+                        new_v = *reinterpret_cast<const uint4 *>(rope.v_new + src);
+                    }
+                } else {
+                    load_q<D, HG, __nv_bfloat16>(q, (size_t)cc.b * Hq + g * G + gs * HG, gl,
+                                                 scale_log2, qp);
+                }
 #pragma unroll
                 for (int h = 0; h < HG; ++h) {
                     m_ref[h] = -INFINITY;
@@ -542,6 +641,24 @@ __global__ void __launch_bounds__(kWarps * 32)
             ok = __all_sync(0xffffffffu,
                             mbar_wait(&bars[warp * kRing + slot], (it / kRing) & 1, &never));
             if (!ok) break;
+            if constexpr (ROPE) {
+                if (cc.off + n == cc.Lb) {  // the stage holds the newest key, as its row n - 1
+                    const int g = cc.sl / SUB;
+                    const uint4 kw = new_k, vw = new_v;
+                    if (grp == 0) {
+                        uint8_t *stg = ring + (warp * kRing + slot) * P::STAGE;
+                        *reinterpret_cast<uint4 *>(stg + (n - 1) * P::ROW + gl * 16) = kw;
+                        *reinterpret_cast<uint4 *>(stg + (SK + n - 1) * P::ROW + gl * 16) = vw;
+                        if (cc.sl % SUB == 0) {
+                            const size_t row =
+                                (((size_t)cc.b * Hkv + g) * max_len + (cc.Lb - 1)) * D + gl * 8;
+                            *reinterpret_cast<uint4 *>(rope.kc + row) = kw;
+                            *reinterpret_cast<uint4 *>(rope.vc + row) = vw;
+                        }
+                    }
+                    __syncwarp();
+                }
+            }
             stage_update<D, HG>(ring + (warp * kRing + slot) * P::STAGE, n, grp, gl, qp, m_ref,
                                 acc, l_own, pw);
             if (last) {
@@ -593,14 +710,14 @@ __global__ void __launch_bounds__(kWarps * 32)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Merge for the stream kernel: one block of kStreamMergeWarps warps per (sequence, query head).
-// Warp w combines pieces w, w + kStreamMergeWarps, ... (in order, eight loads in flight at a
+// Merge for the stream kernel: one block of MW warps per (sequence, query head).
+// Warp w combines pieces w, w + MW, ... (in order, eight loads in flight at a
 // time); the warp results are then combined in warp order through shared memory, so the result
 // does not depend on timing.
-constexpr int kStreamMergeWarps = 16;
-
-template <bool OUT_F32, int D, int HG>
-__global__ void __launch_bounds__(kStreamMergeWarps * 32)
+// MW warps per block: 16 when there are few streams (each with many pieces), 4 when there are
+// many (each with few pieces, and the narrower blocks all fit on the GPU at once).
+template <bool OUT_F32, int D, int HG, int MW>
+__global__ void __launch_bounds__(MW * 32)
     decode_stream_merge_kernel(const float *__restrict__ ws_o, const float2 *__restrict__ ws_ml,
                                const int *__restrict__ seqlens, void *__restrict__ o,
                                float *__restrict__ lse, int B, int Hq, int Hkv, int max_len,
@@ -608,7 +725,6 @@ __global__ void __launch_bounds__(kStreamMergeWarps * 32)
 {
     constexpr int DL = D / 32;
     constexpr int PW = 8;  // pieces per warp per round
-    constexpr int MW = kStreamMergeWarps;
     __shared__ float s_acc[MW][D];
     __shared__ float s_m[MW], s_l[MW];
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -849,10 +965,11 @@ int largest_group(int G)
     return G % 8 == 0 ? 8 : (G % 4 == 0 ? 4 : (G % 2 == 0 ? 2 : 1));
 }
 
-template <int D, int HG, typename QT>
+template <int D, int HG, bool ROPE>
 cudaError_t launch_stream_t(const DecodeArgs &a, bool out_f32, cudaStream_t st)
 {
     using P = Plan<D, HG>;
+    constexpr auto kern = decode_stream_kernel<D, HG, ROPE>;
     static bool attr_set[64] = {};
     static int blocks_cached[64] = {};
     int dev = 0;
@@ -860,14 +977,14 @@ cudaError_t launch_stream_t(const DecodeArgs &a, bool out_f32, cudaStream_t st)
     if (e != cudaSuccess) return e;
     int blocks = dev < 64 ? blocks_cached[dev] : 0;
     if (dev >= 64 || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(decode_stream_kernel<D, HG, QT>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, P::RING + P::PBUF + P::BARS);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 P::RING + P::PBUF + P::BARS);
         if (e != cudaSuccess) return e;
         int sms = 0, occ = 0;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_stream_kernel<D, HG, QT>,
-                                                          kWarps * 32, P::RING + P::PBUF + P::BARS);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kWarps * 32,
+                                                          P::RING + P::PBUF + P::BARS);
         if (e != cudaSuccess) return e;
         blocks = sms * (occ > 0 ? occ : 1);
         if (blocks * kWarps > kStreamMaxWarps) blocks = kStreamMaxWarps / kWarps;
@@ -879,15 +996,24 @@ cudaError_t launch_stream_t(const DecodeArgs &a, bool out_f32, cudaStream_t st)
     float *ws_o = static_cast<float *>(a.ws);
     const size_t rows = (size_t)kStreamMaxWarps * HG + (size_t)a.B * a.Hq;
     float2 *ws_ml = reinterpret_cast<float2 *>(ws_o + rows * D);
-    e = launch_pdl(decode_stream_kernel<D, HG, QT>, dim3(blocks), dim3(kWarps * 32),
-                   P::RING + P::PBUF + P::BARS, st, static_cast<const QT *>(a.q),
-                   static_cast<const __nv_bfloat16 *>(a.kc),
+    RopeIn rope = {};
+    if (ROPE) {
+        rope.k_new = static_cast<const __nv_bfloat16 *>(a.k_new);
+        rope.v_new = static_cast<const __nv_bfloat16 *>(a.v_new);
+        rope.cos_t = a.cos_t;
+        rope.sin_t = a.sin_t;
+        rope.kc = static_cast<__nv_bfloat16 *>(const_cast<void *>(a.kc));
+        rope.vc = static_cast<__nv_bfloat16 *>(const_cast<void *>(a.vc));
+    }
+    e = launch_pdl(kern, dim3(blocks), dim3(kWarps * 32), P::RING + P::PBUF + P::BARS, st,
+                   static_cast<const __nv_bfloat16 *>(a.q), static_cast<const __nv_bfloat16 *>(a.kc),
                    static_cast<const __nv_bfloat16 *>(a.vc), a.seqlens, ws_o, ws_ml, a.B, a.Hq,
-                   a.Hkv, a.max_len, a.scale_log2, a.status);
+                   a.Hkv, a.max_len, a.scale_log2, a.status, rope);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
+    const bool many = (long long)a.B * a.Hkv * (a.Hq / a.Hkv / HG) >= 128;  // streams
     cfg.gridDim = dim3(a.B * a.Hq);
-    cfg.blockDim = dim3(kStreamMergeWarps * 32);
+    cfg.blockDim = dim3((many ? 4 : 16) * 32);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -895,23 +1021,22 @@ cudaError_t launch_stream_t(const DecodeArgs &a, bool out_f32, cudaStream_t st)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const int nwt = blocks * kWarps;
-    if (out_f32)
-        return cudaLaunchKernelEx(&cfg, decode_stream_merge_kernel<true, D, HG>, (const float *)ws_o,
-                                  (const float2 *)ws_ml, a.seqlens, a.o, a.lse, a.B, a.Hq, a.Hkv,
-                                  a.max_len, nwt);
-    return cudaLaunchKernelEx(&cfg, decode_stream_merge_kernel<false, D, HG>, (const float *)ws_o,
-                              (const float2 *)ws_ml, a.seqlens, a.o, a.lse, a.B, a.Hq, a.Hkv,
-                              a.max_len, nwt);
+    auto merge = out_f32 ? (many ? decode_stream_merge_kernel<true, D, HG, 4>
+                                 : decode_stream_merge_kernel<true, D, HG, 16>)
+                         : (many ? decode_stream_merge_kernel<false, D, HG, 4>
+                                 : decode_stream_merge_kernel<false, D, HG, 16>);
+    return cudaLaunchKernelEx(&cfg, merge, (const float *)ws_o, (const float2 *)ws_ml, a.seqlens,
+                              a.o, a.lse, a.B, a.Hq, a.Hkv, a.max_len, nwt);
 }
 
-template <int D, typename QT>
+template <int D, bool ROPE>
 cudaError_t launch_stream_d(const DecodeArgs &a, bool out_f32, cudaStream_t st)
 {
     switch (largest_group(a.Hq / a.Hkv)) {
-    case 8: return launch_stream_t<D, 8, QT>(a, out_f32, st);
-    case 4: return launch_stream_t<D, 4, QT>(a, out_f32, st);
-    case 2: return launch_stream_t<D, 2, QT>(a, out_f32, st);
-    default: return launch_stream_t<D, 1, QT>(a, out_f32, st);
+    case 8: return launch_stream_t<D, 8, ROPE>(a, out_f32, st);
+    case 4: return launch_stream_t<D, 4, ROPE>(a, out_f32, st);
+    case 2: return launch_stream_t<D, 2, ROPE>(a, out_f32, st);
+    default: return launch_stream_t<D, 1, ROPE>(a, out_f32, st);
     }
 }
 
@@ -965,6 +1090,8 @@ __global__ void __launch_bounds__(D / 2)
 
 }  // namespace
 
+bool decode_fuses_rope(int B) { return B <= kStreamMaxBatch; }
+
 int decode_chunk_len(int B, int Hkv, int max_len)
 {
     // Chunked kernel (batches above the stream kernel's limit): aim for about three blocks per
@@ -994,12 +1121,14 @@ cudaError_t launch_decode(const DecodeArgs &a0, bool out_f32, cudaStream_t st)
 {
     DecodeArgs a = a0;
     if (a.B <= kStreamMaxBatch) {
-        if (a.q_f32)
-            return a.D == 128 ? launch_stream_d<128, float>(a, out_f32, st)
-                              : launch_stream_d<64, float>(a, out_f32, st);
-        return a.D == 128 ? launch_stream_d<128, __nv_bfloat16>(a, out_f32, st)
-                          : launch_stream_d<64, __nv_bfloat16>(a, out_f32, st);
+        if (a.q_f32) return cudaErrorInvalidValue;  // the stream kernel takes a bf16 q
+        if (a.k_new != nullptr)
+            return a.D == 128 ? launch_stream_d<128, true>(a, out_f32, st)
+                              : launch_stream_d<64, true>(a, out_f32, st);
+        return a.D == 128 ? launch_stream_d<128, false>(a, out_f32, st)
+                          : launch_stream_d<64, false>(a, out_f32, st);
     }
+    if (a.k_new != nullptr) return cudaErrorInvalidValue;  // RoPE runs as its own kernel here
     a.chunk = decode_chunk_len(a.B, a.Hkv, a.max_len);
     a.nsplit = (a.max_len + a.chunk - 1) / a.chunk;
     a.ws_o = static_cast<float *>(a.ws);

@@ -56,12 +56,21 @@ struct DecodeArgs {
     float scale_log2;
     unsigned *status;
     bool q_f32 = false;   // q is fp32 (the RoPE step's output) instead of bf16
+    // decode with RoPE fused into the stream kernel (batches up to 1024): the new token's key
+    // and value [B, Hkv, D] bf16 and the angle tables [max_len, D/2] fp32, all 16-byte aligned;
+    // q is then the unrotated bf16 query. nullptr: plain decode.
+    const void *k_new = nullptr, *v_new = nullptr;
+    const float *cos_t = nullptr, *sin_t = nullptr;
     // filled in by launch_decode for the chunked kernel
     float *ws_o = nullptr;
     float2 *ws_ml = nullptr;
     int chunk = 0, nsplit = 0;
 };
 cudaError_t launch_decode(const DecodeArgs &a, bool out_f32, cudaStream_t stream);
+
+// Whether launch_decode can fuse RoPE and the cache store into its kernel for batch B (else
+// launch_rope_append runs first and the decode reads its fp32 q).
+bool decode_fuses_rope(int B);
 
 // RoPE (rotate-half) of the new token of each sequence at position seqlens[b] - 1: q into
 // q_rot [B, Hq, D] fp32; k_new rotated and v_new stored at that row of the caches.

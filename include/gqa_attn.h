@@ -220,8 +220,13 @@ int attn_decode_noalloc(const void *q, const void *kcache, const void *vcache, c
  *   kcache, vcache [B, Hkv, max_len, D] bf16, row seqlens[b]-1 overwritten
  *   seqlens [B] int32 (device): lengths including the new token
  *   o [B, Hq, D] bf16 or fp32 by out_dtype, lse [B, Hq] fp32 or NULL
- * Scratch (partials and the rotated queries) comes from the library-owned buffer, grown on
- * first use as for attn_decode. Requires D in {64, 128}.
+ * q, k_new, v_new, cos_t, sin_t must be 16-byte aligned (else ATTN_ERR_ALIGN).
+ * Batches up to 1024: one kernel does everything. The query is rotated as it is loaded; the
+ * warp whose key slice ends a sequence substitutes the rotated key (rounded to bf16) and the
+ * value for the cache row it just read, and writes both to the cache. Larger batches: a small
+ * kernel rotates q (kept in fp32) and stores the key and value first, then the decode runs.
+ * Scratch (partials; the rotated queries for large batches) comes from the library-owned
+ * buffer, grown on first use as for attn_decode. Requires D in {64, 128}.
  * Sources: "triton-optimization" skill (skillsmp.com) section 3.4 (RoPE on the two halves of a
  * head with precomputed cos/sin tables, q and k in one kernel); "Hand-written Triton decoder"
  * (m.nlpx.cn/news/28229) section 1.2 (RoPE computed in fp32 while q and k are loaded) and

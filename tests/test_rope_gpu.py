@@ -1,5 +1,6 @@
-"""Decode step with the new token's RoPE and cache store (rope kernel + split-KV decode, through
-the C ABI) against the fp64 oracle on the same seeded inputs."""
+"""Decode step with the new token's RoPE and cache store (through the C ABI) against the fp64
+oracle on the same seeded inputs: fused into the stream kernel for batches up to 1024, a rope
+kernel before the chunked decode above that."""
 import math
 
 import numpy as np
@@ -19,14 +20,25 @@ def _tables(max_len, D, base=10000.0):
     return torch.cos(ang).float(), torch.sin(ang).float()
 
 
+def _lens_1100():
+    lens = torch.randint(0, 97, (1100,), generator=torch.Generator().manual_seed(9))
+    lens[::11] = 0
+    return lens.tolist()
+
+
 @pytest.mark.parametrize("B,Hq,Hkv,D,max_len,lens", [
     (4, 8, 2, 128, 4096, [4096, 1, 1000, 2]),
     (32, 8, 2, 128, 4096, None),
     (3, 16, 2, 64, 700, [700, 350, 1]),
+    (3, 12, 2, 128, 500, [500, 1, 250]),     # three query-head subgroups share each kv head
+    (4, 8, 2, 128, 300, [0, 300, 17, 1]),    # an empty sequence stores nothing
+    (1100, 8, 2, 128, 96, "b1100"),          # above 1024: rope kernel, then chunked decode
 ])
 def test_decode_rope_parity(B, Hq, Hkv, D, max_len, lens):
     cga = library()
     dev = device()
+    if lens == "b1100":
+        lens = _lens_1100()
     q, kc, vc, sl = workloads.decode_inputs(B, Hq, Hkv, D, max_len,
                                             "uniform" if lens is None else "explicit", seed=7,
                                             seqlens=lens)
@@ -48,11 +60,18 @@ def test_decode_rope_parity(B, Hq, Hkv, D, max_len, lens):
     check_out(o, o_ref, "bf16_pre", tag)
     check_lse(lse, lse_ref, tag + " lse")
     # the stored key row equals the oracle's rounding within one bf16 step, the value exactly
+    kca, vca = kcd.cpu(), vcd.cpu()
+    untouched = torch.ones((B, max_len), dtype=torch.bool)
     for b in range(B):
         p = int(sl[b]) - 1
         if p < 0:
             continue
-        krow = kcd[b, :, p].double().cpu().numpy()
+        untouched[b, p] = False
+        krow = kca[b, :, p].double().numpy()
         assert np.all(np.abs(krow - krow_ref[b]) <= bf16_ulp(krow_ref[b]) + 1e-30), "k row"
-        assert torch.equal(vcd[b, :, p].cpu(), vn[b]), "v row"
+        assert torch.equal(vca[b, :, p], vn[b]), "v row"
+    # every other cache row keeps its bits (NaN past each length included)
+    for before, after in ((kc, kca), (vc, vca)):
+        same = before.view(torch.int16) == after.view(torch.int16)
+        assert bool(same.all(dim=-1).permute(0, 2, 1)[untouched].all()), "other cache rows changed"
     assert cga.device_status() == 0
