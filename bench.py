@@ -58,7 +58,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-extras", action="store_true",
-                   help="skip the extra timings (cache chunk, padded varlen prefill, decode with RoPE)")
+                   help="skip the extra timings (cache chunk, padded varlen, fused-QKV and "
+                        "head-dim-64 prefill, decode with RoPE)")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle sample")
     p.add_argument("--only", default="all", choices=["all", "prefill", "decode"],
@@ -345,6 +346,26 @@ def time_extras(cga, dev, stream, flush, steps):
     fl = sum(workloads.prefill_flops(1, Hq, int(L), D, True) for L in lens.tolist())
     out["varlen_b8_s1024to8192_padded8192"] = {"ms": ms, "value": fl / (ms * 1e-3) / 1e12,
                                                "unit": "TFLOP/s", "flops": fl}
+    del q, k, v, o
+    # prefill read in place from a fused QKV projection output [B, S, Hq + 2 Hkv, D], O written
+    # as [B, S, Hq, D]; and head dim 64 (both B8 S8192 Hq8 Hkv2 causal)
+    S = 8192
+    fl = workloads.prefill_flops(B, Hq, S, D, True)
+    x = torch.randn((B, S, Hq + 2 * Hkv, D), generator=g).to(torch.bfloat16).to(dev)
+    qv, kv, vv = (x[:, :, :Hq].transpose(1, 2), x[:, :, Hq:Hq + Hkv].transpose(1, 2),
+                  x[:, :, Hq + Hkv:].transpose(1, 2))
+    ov = torch.empty((B, S, Hq, D), dtype=torch.bfloat16, device=dev).transpose(1, 2)
+    ms = _time(lambda: cga.prefill(qv, kv, vv, causal=True, out=ov), flush, stream,
+               max(3, steps // 2))
+    out["prefill_fused_qkv_b8_s8192"] = {"ms": ms, "value": fl / (ms * 1e-3) / 1e12,
+                                         "unit": "TFLOP/s", "flops": fl}
+    del x, qv, kv, vv, ov
+    q, k, v = [t.to(dev) for t in workloads.prefill_inputs(B, Hq, Hkv, S, 64, "bf16", seed=4)]
+    o = torch.empty_like(q)
+    fl = workloads.prefill_flops(B, Hq, S, 64, True)
+    ms = _time(lambda: cga.prefill(q, k, v, causal=True, out=o), flush, stream, max(3, steps // 2))
+    out["prefill_d64_b8_s8192"] = {"ms": ms, "value": fl / (ms * 1e-3) / 1e12,
+                                   "unit": "TFLOP/s", "flops": fl}
     del q, k, v, o
     # decode step with RoPE of the new token and its cache store (32 sequences of 256..4096),
     # beside the plain decode of the same caches
