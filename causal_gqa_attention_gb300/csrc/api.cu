@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 // Per-device status word written by the kernels (bits ATTN_DEV_*).
 __device__ unsigned int g_attn_status;
@@ -99,10 +100,14 @@ int status_ptr(unsigned **out)
     return ATTN_OK;
 }
 
-// ---- library-owned decode workspace, per device
+// ---- library-owned scratch, per device. Growing it allocates a new buffer and keeps the old
+// one for the life of the process: a CUDA graph captured with the old buffer keeps replaying on
+// valid memory, and no kernel still in flight can see its buffer freed. Sizes at least double,
+// so the retained buffers add up to less than the current one.
 struct Workspace {
     void *ptr = nullptr;
     size_t bytes = 0;
+    std::vector<void *> retired;
 };
 Workspace g_ws[kMaxDevices];
 std::mutex g_ws_mu;
@@ -118,17 +123,12 @@ int workspace_acquire(size_t need, cudaStream_t stream, bool may_grow, void **ou
         cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
         if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return ATTN_ERR_CUDA;
         if (cs != cudaStreamCaptureStatusNone) return ATTN_ERR_WORKSPACE;
-        if (w.ptr) {
-            if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
-            cudaFree(w.ptr);
-            w.ptr = nullptr;
-            w.bytes = 0;
-        }
         size_t sz = need < (1u << 20) ? (1u << 20) : need;
-        if (cudaMalloc(&w.ptr, sz) != cudaSuccess) {
-            w.ptr = nullptr;
-            return ATTN_ERR_CUDA;
-        }
+        if (sz < 2 * w.bytes) sz = 2 * w.bytes;
+        void *p = nullptr;
+        if (cudaMalloc(&p, sz) != cudaSuccess) return ATTN_ERR_CUDA;
+        if (w.ptr) w.retired.push_back(w.ptr);
+        w.ptr = p;
         w.bytes = sz;
     }
     *out = w.ptr;

@@ -168,10 +168,11 @@ int attn_prefill_varlen(const void *q, const void *k, const void *v, const int *
  *   o        [B, Hq, D] bf16
  * Requires Hq % Hkv == 0, D in {64, 128}, max_len >= 1.
  * Scratch for the per-chunk partial results comes from a library-owned buffer per device.
- * The first call for a larger shape grows it (cudaMalloc, with a device synchronisation);
- * during stream capture it cannot grow and the call returns ATTN_ERR_WORKSPACE instead, so
- * reserve it first with attn_reserve_workspace. Calls on different streams of one device
- * share that buffer: serialise them, or use attn_decode_ex with your own workspace.
+ * The first call for a larger shape grows it: cudaMalloc of a new buffer at least twice as
+ * large; the old one stays allocated until the process exits, so CUDA graphs captured with it
+ * remain valid. During stream capture it cannot grow and the call returns ATTN_ERR_WORKSPACE
+ * instead, so reserve it first with attn_reserve_workspace. Calls on different streams of one
+ * device share that buffer: serialise them, or use attn_decode_ex with your own workspace.
  */
 int attn_decode(const void *q, const void *kcache, const void *vcache, const int *seqlens,
                 void *o, int B, int Hq, int Hkv, int D, int max_len, float scale, void *stream);
@@ -245,7 +246,8 @@ size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int max_len);
 int attn_decode_chunk_len(int B, int Hkv, int max_len);
 
 /* Grow the library-owned decode workspace of the current device to fit this shape. Call it
- * before capturing attn_decode in a CUDA graph. Synchronises the device when it grows. */
+ * before capturing attn_decode in a CUDA graph (a graph keeps the buffer it was captured with;
+ * growing later allocates a new one and keeps the old). */
 int attn_reserve_workspace(int B, int Hq, int Hkv, int D, int max_len);
 
 /* Synchronise `stream`, then read and clear the current device's status word into *status
