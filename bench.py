@@ -198,6 +198,15 @@ def max_over_ranks(x: float, world: int, dev) -> float:
     return float(t.item())
 
 
+def whole_job_rate(units_per_rank: float, local_ms: float, world: int, dev):
+    """Weak scaling: every rank processes units_per_rank in local_ms. Returns the slowest rank's
+    time (ms), the per-GPU rate at that time and the whole-job rate (all ranks' units over the
+    slowest time), rates in units per second."""
+    ms = max_over_ranks(local_ms, world, dev)
+    per_gpu = units_per_rank / (max(ms, 1e-6) * 1e-3)
+    return ms, per_gpu, per_gpu * world
+
+
 # --------------------------------------------------------------------------- oracle sample
 
 
@@ -467,11 +476,11 @@ def main():
 
     pre_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.steps)]
     dec_ms = [ev[s][2].elapsed_time(ev[s][3]) for s in range(args.steps)]
-    pre_mean = max_over_ranks(sum(pre_ms) / len(pre_ms), world, dev)
-    dec_mean = max_over_ranks(sum(dec_ms) / len(dec_ms), world, dev)
+    pre_mean, pre_rate, pre_job = whole_job_rate(pflops, sum(pre_ms) / len(pre_ms), world, dev)
+    dec_mean, dec_rate, _ = whole_job_rate(dec_bytes, sum(dec_ms) / len(dec_ms), world, dev)
     step_ms = pre_mean + dec_mean
-    tflops = pflops / (max(pre_mean, 1e-6) * 1e-3) / 1e12
-    dec_gbs = dec_bytes / (max(dec_mean, 1e-6) * 1e-3) / 1e9
+    tflops = pre_rate / 1e12
+    dec_gbs = dec_rate / 1e9
 
     # ---- decode, back to back: a CUDA graph of DECODE_CALLS calls over DECODE_SETS caches
     b2b = None
@@ -574,7 +583,7 @@ def main():
         traffic = recorded_traffic()
         line = {
             "metric": METRIC,
-            "value": tflops * world,
+            "value": pre_job / 1e12,
             "unit": "TFLOP/s",
             "n_gpus": world,
             "steps": args.steps,
