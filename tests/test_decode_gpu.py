@@ -73,15 +73,22 @@ def test_decode_empty_sequence():
 
 
 def test_decode_caller_workspace_and_determinism():
+    """A caller workspace takes the separate merge kernel, the library's scratch the merge inside
+    the stream kernel (per-stream key counters, reset by the warp that completes a stream): both
+    agree with the oracle, and each gives identical bits on every call."""
     cga = library()
     dev = device()
     cfg = workloads.CONFIGS["c4b"]
     q, kc, vc, sl = workloads.config_decode_inputs(cfg)
+    o_ref, lse_ref = oracle.decode(q, kc, vc, sl, cfg.scale)
     nbytes = cga.attn_decode_workspace_bytes(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, cfg.max_len)
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-    o1, _ = _run(q, kc, vc, sl, torch.bfloat16, workspace=ws)
-    o2, _ = _run(q, kc, vc, sl, torch.bfloat16)
-    assert torch.equal(o1, o2)
+    for kw in ({"workspace": ws}, {}):
+        runs = [_run(q, kc, vc, sl, torch.float32, **kw) for _ in range(3)]
+        for o, lse in runs[1:]:
+            assert torch.equal(o, runs[0][0]) and torch.equal(lse, runs[0][1])
+        check_out(runs[0][0], o_ref, "bf16_pre", f"c4b {list(kw)}")
+        check_lse(runs[0][1], lse_ref, f"c4b lse {list(kw)}")
     small = torch.empty(nbytes - 16, dtype=torch.uint8, device=dev)
     with pytest.raises(cga.AttnError) as ei:
         _run(q, kc, vc, sl, torch.bfloat16, workspace=small)
