@@ -44,7 +44,13 @@
 #include "internal.h"
 #include "ptx.cuh"
 
+#include <algorithm>
+#include <array>
 #include <cmath>
+#include <map>
+#include <mutex>
+#include <queue>
+#include <vector>
 
 namespace gqa {
 namespace {
@@ -114,11 +120,21 @@ __host__ __device__ __forceinline__ int rb_key_tiles(int rb, int S, int causal)
 }
 
 // Split mode: row block rb is cut into ceil(tiles / J) segments of at most J key tiles, each
-// one block. Blocks are numbered heaviest row block first: all segments of row block n_rb - 1
-// (segment-major, then batch x head), then n_rb - 2, ...
+// one block. Every row block gets the same number of segment slots, NS (the longest row
+// block's segment count), so block -> (row block, segment, head) is plain arithmetic: blocks
+// are numbered heaviest row block first (row block n_rb - 1 - blockIdx / (NS * heads)), then
+// segment, then batch x head. Slots past a row block's segments exit at once.
 __host__ __device__ __forceinline__ int rb_segments(int rb, int S, int causal, int J)
 {
     return (rb_key_tiles(rb, S, causal) + J - 1) / J;
+}
+
+// Segment slots per row block in split mode: the most segments any row block has.
+__host__ __device__ __forceinline__ int split_slots(int S, int causal, int J)
+{
+    const int n_rb = (S + 2 * BM - 1) / (2 * BM);
+    const int a = rb_segments(n_rb - 1, S, causal, J), b = rb_segments(0, S, causal, J);
+    return a > b ? a : b;
 }
 
 // 1 if either bf16 half of w has magnitude >= 2^16 (beyond the fp16 range) or is inf/NaN.
@@ -151,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       float *__restrict__ lse, int B, int S, int Hq, int Hkv, float scale_log2,
                       int causal, unsigned *__restrict__ status, int J, float *__restrict__ ws_o,
                       float *__restrict__ ws_lse, const int *__restrict__ kv_lens, int max_kv,
-                      int front, long long o_sb, long long o_ss, long long o_sh)
+                      int front, long long o_sb, long long o_ss, long long o_sh, int NS)
 {
     using G = Geo<HD>;
     constexpr uint32_t kTile = G::kTile, kOffQ = G::kOffQ, kOffK = G::kOffK, kOffV = G::kOffV,
@@ -172,14 +188,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         rb = n_rb - 1 - (int)blockIdx.x / (Hq * B);
         hb = (int)blockIdx.x % (Hq * B);
     } else {
-        int rem = (int)blockIdx.x;
-        for (rb = n_rb - 1; rb > 0; --rb) {
-            const int c = rb_segments(rb, S, causal, J) * Hq * B;
-            if (rem < c) break;
-            rem -= c;
-        }
+        const int per_rb = NS * Hq * B;
+        rb = n_rb - 1 - (int)blockIdx.x / per_rb;
+        const int rem = (int)blockIdx.x % per_rb;
         seg = rem / (Hq * B);
         hb = rem % (Hq * B);
+        if (seg >= rb_segments(rb, S, causal, J)) return;  // empty slot: nothing set up yet
     }
     const int h = hb % Hq, b = hb / Hq;
     const int g = h / (Hq / Hkv);
@@ -466,7 +480,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool active = hi[t] >= jb;  // warp-uniform
             if (ok && active)
                 ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_OFULL + t], 0, abort_flag));
-            if (ok && SPLIT) {
+            // a row block whose keys fit in one segment writes its final result directly
+            const bool direct = SPLIT && rb_segments(rb, S, causal, J) == 1;
+            if (ok && SPLIT && !direct) {
                 // segment result: normalised O (fp32) and LSE in log2 units; an empty segment
                 // (this tile has no key tile in it) writes O = 0 and LSE = -inf
                 if (active) tc_fence_after();
@@ -552,7 +568,7 @@ __global__ void __launch_bounds__(256)
     prefill_split_merge_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_lse,
                                void *__restrict__ out, float *__restrict__ lse, int B, int S,
                                int Hq, int causal, int J, long long o_sb, long long o_ss,
-                               long long o_sh)
+                               long long o_sh, int NS)
 {
     constexpr int DPL = HD / 32;  // dims per lane: 4 or 2
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -563,9 +579,9 @@ __global__ void __launch_bounds__(256)
     const int hb = (int)(row / S);  // b * Hq + h
     const int n_rb = (S + 2 * BM - 1) / (2 * BM);
     const int rb = i / (2 * BM), rloc = i % (2 * BM);
-    int first = 0;  // first block of row block rb
-    for (int r2 = n_rb - 1; r2 > rb; --r2) first += rb_segments(r2, S, causal, J) * Hq * B;
+    const int first = (n_rb - 1 - rb) * NS * Hq * B;  // first block of row block rb
     const int nseg = rb_segments(rb, S, causal, J);
+    if (nseg == 1) return;  // that row block wrote its result itself
     // every load of the row in one round: segment LSEs and this lane's dims of each O
     float ls[8];
     float4 x[8];
@@ -641,14 +657,12 @@ cudaError_t launch_t(const PrefillTcArgs &a, cudaStream_t st)
     }
     const int n_rb = (a.S + 2 * BM - 1) / (2 * BM);
     long long blocks = (long long)n_rb * a.Hq * a.B;
-    if (SPLIT) {
-        blocks = 0;
-        for (int rb = 0; rb < n_rb; ++rb) blocks += (long long)rb_segments(rb, a.S, a.causal, a.J) * a.Hq * a.B;
-    }
+    const int NS = SPLIT ? split_slots(a.S, a.causal, a.J) : 1;
+    if (SPLIT) blocks = (long long)n_rb * NS * a.Hq * a.B;
     prefill_tc_kernel<HD, OUT_F32, SPLIT><<<(unsigned)blocks, kThreads, Geo<HD>::kSmem, st>>>(
         a.tq, a.tk, a.tv, a.o, a.lse, a.B, a.S, a.Hq, a.Hkv, a.scale_log2, a.causal, a.status,
         a.J, a.ws_o, a.ws_lse, a.kv_lens, a.kv_lens ? a.max_kv : a.S, a.front, a.o_sb, a.o_ss,
-        a.o_sh);
+        a.o_sh, NS);
     e = cudaGetLastError();
     if (e != cudaSuccess || !SPLIT) return e;
     const long long rows = (long long)a.B * a.Hq * a.S;
@@ -663,7 +677,7 @@ cudaError_t launch_t(const PrefillTcArgs &a, cudaStream_t st)
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, prefill_split_merge_kernel<HD, OUT_F32>, (const float *)a.ws_o,
                               (const float *)a.ws_lse, a.o, a.lse, a.B, a.S, a.Hq, a.causal, a.J,
-                              a.o_sb, a.o_ss, a.o_sh);
+                              a.o_sb, a.o_ss, a.o_sh, NS);
 }
 
 template <int HD>
@@ -685,31 +699,80 @@ cudaError_t launch_prefill_tc(const PrefillTcArgs &a, bool out_f32, cudaStream_t
 
 size_t prefill_split_plan(int B, int S, int Hq, int D, int causal, int num_sms, int *J_out)
 {
-    // Split the key range only when the plain grid leaves SMs idle: pick the longest segment
-    // (fewest blocks) whose grid still fits in one wave; at most 8 segments per row block.
+    // Splitting the key range of the long (causal: the late) row blocks into segments of J key
+    // tiles evens out the blocks' work when the grid is only a few waves deep. The choice is an
+    // estimate of the finishing time: blocks (one per SM at a time, heaviest first, as launched)
+    // are list-scheduled on the SMs at a cost of their key tiles plus a fixed start-up and
+    // write-out cost, plus the traffic of the partial results of the split row blocks and the
+    // merge launch. Row blocks left in one segment write their result directly. At most 8
+    // segments per row block (the merge kernel reads up to 8).
     *J_out = 0;
     const int n_rb = (S + 2 * BM - 1) / (2 * BM);
-    const long long plain = (long long)n_rb * Hq * B;
-    if (plain >= num_sms) return 0;
-    const int nmax = rb_key_tiles(n_rb - 1, S, causal) > rb_key_tiles(0, S, causal)
-                         ? rb_key_tiles(n_rb - 1, S, causal)
-                         : rb_key_tiles(0, S, causal);
+    const long long heads = (long long)Hq * B;
+    if ((long long)n_rb * heads >= 4LL * num_sms || num_sms <= 0) return 0;
+    static std::mutex mu;
+    static std::map<std::array<long long, 6>, int> cache;
+    const std::array<long long, 6> key = {B, S, Hq, D, causal, num_sms};
     int best = 0;
-    for (int J = nmax - 1; J >= 2; --J) {
-        long long blocks = 0;
-        bool fits = true;
-        for (int rb = 0; rb < n_rb; ++rb) {
-            const int ns = rb_segments(rb, S, causal, J);
-            if (ns > 8) fits = false;
-            blocks += (long long)ns * Hq * B;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) {
+            best = it->second;
+        } else {
+            // Cost model in key-tile steps (one step about 1.9 us), fitted to measured
+            // B1-B2 S2048-8192 causal timings over several split lengths: a block costs its
+            // steps plus 4 (start-up: TMEM, barriers, Q and first K/V loads; write-out); a
+            // split adds about 2 steps (merge launch and dependency wait) and 1e-4 step per
+            // row of a split row block (partials written, read back and merged).
+            constexpr double kStart = 4.0;
+            constexpr double kMerge = 2.1;
+            constexpr double kRowSteps = 1.05e-4;
+            int nmax = 0;
+            for (int rb = 0; rb < n_rb; ++rb) nmax = std::max(nmax, rb_key_tiles(rb, S, causal));
+            std::vector<double> load;
+            auto estimate = [&](int J) {
+                load.assign(num_sms, 0.0);
+                std::priority_queue<double, std::vector<double>, std::greater<double>> q(
+                    load.begin(), load.end());
+                double rows_split = 0.0;
+                for (int rb = n_rb - 1; rb >= 0; --rb) {
+                    const int t = rb_key_tiles(rb, S, causal);
+                    const int ns = J > 0 ? (t + J - 1) / J : 1;
+                    if (ns > 1) rows_split += 2.0 * BM * heads * ns;
+                    for (int k = 0; k < ns; ++k) {
+                        const int len = J > 0 ? std::min(J, t - k * J) : t;
+                        for (long long h = 0; h < heads; ++h) {
+                            const double at = q.top();
+                            q.pop();
+                            q.push(at + len + kStart);
+                        }
+                    }
+                }
+                double end = 0.0;
+                while (!q.empty()) {
+                    end = std::max(end, q.top());
+                    q.pop();
+                }
+                return end + (J > 0 ? kMerge : 0.0) + rows_split * kRowSteps;
+            };
+            // a split must promise a tenth off the unsplit estimate (the model's error is a
+            // few percent)
+            const double plain = estimate(0);
+            double best_t = 0.9 * plain;
+            for (int J = std::max(2, (nmax + 7) / 8); J < nmax; ++J) {
+                const double t = estimate(J);
+                if (t < best_t) {
+                    best_t = t;
+                    best = J;
+                }
+            }
+            cache[key] = best;
         }
-        if (!fits || blocks > num_sms) break;
-        best = J;
     }
     if (best == 0) return 0;
     *J_out = best;
-    long long blocks = 0;
-    for (int rb = 0; rb < n_rb; ++rb) blocks += (long long)rb_segments(rb, S, causal, best) * Hq * B;
+    const long long blocks = (long long)n_rb * split_slots(S, causal, best) * heads;
     return (size_t)blocks * (2 * BM) * (D + 1) * sizeof(float);
 }
 
