@@ -4,9 +4,10 @@
 // (the [B, H, S, D] default, [B, S, H, D], or q/k/v as slices of one fused projection output).
 //
 // One thread block owns 256 consecutive query rows of one (batch, query head): two 128-row
-// Q tiles. Both tiles consume the same stream of 128-key K/V tiles, so every K/V tile brought
-// in by TMA feeds four 128x128x128 tensor-core products. Roles (12 warps):
-//   warp 0      TMA producer: Q tiles once, then K_j and V_j into a 2-stage ring each;
+// Q tiles (HD = 128; half as wide at 64). Both tiles consume the same stream of 128-key K/V
+// tiles, so every K/V tile brought in by TMA feeds four tensor-core products. Roles (12 warps):
+//   warp 0      TMA producer: Q tiles once, then K_j into a 2-stage and V_j into a 3-stage ring
+//               (V also waits for its conversion, so it gets one stage more);
 //   warp 1      tcgen05 issuer (one thread): S_t = Q_t K_j^T into TMEM, O_t += P_t V_j with
 //               P_t read from TMEM; owns the TMEM allocation;
 //   warps 2-3   convert each landed V tile from bf16 to fp16 in place (see below);
@@ -14,8 +15,8 @@
 //               lane). Reads the 128 scores of its row, masks, updates the running max and
 //               sum, writes P (fp16) over the scores it came from, rescales its O row when
 //               the max moved, and finally writes O / l and the LSE.
-// TMEM (512 columns): S_0 | S_1 | O_0 | O_1, 128 fp32 columns each; P_t is packed fp16 in the
-// first 64 columns of S_t. S and P never leave the SM.
+// TMEM (512 columns): S_0 | S_1 | O_0 | O_1, 128 fp32 columns each (O uses HD of them); P_t is
+// packed fp16 in the first 64 columns of S_t. S and P never leave the SM.
 //
 // Precision of the P V product: P is rounded to a 16-bit type before the tensor core consumes
 // it. With bf16 (8-bit significand) a peaky softmax (a few keys carrying most of the weight)
