@@ -62,6 +62,9 @@ constexpr int kThreads = 384;  // 12 warps
 constexpr uint32_t kBox = 16384;          // one 128-row x 64-col bf16 box (128-byte rows)
 constexpr int KST = 2;                    // K ring stages
 constexpr int VST = 3;                    // V ring stages (V also waits for its fp16 conversion)
+// K_jj reuses K_jj-2's stage (read by the scores of step jj - 2) and V_jj reuses V_jj-3's (read by
+// the P V of step jj - 2): one "step jj - 2 done" barrier covers both.
+static_assert(KST == 2 && VST == 3, "stage reuse tied to step jj - 2");
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
 
 // Shared-memory plan for head dim HD (64 or 128): two Q tiles, the K ring, the V ring, then the
@@ -87,10 +90,10 @@ constexpr uint32_t kColO = 256;  // + 128 t
 enum : int {
     B_Q = 0,
     B_KFULL = 1,                // KST
-    B_KEMPTY = B_KFULL + KST,   // KST
-    B_VFULL = B_KEMPTY + KST,   // VST
-    B_VEMPTY = B_VFULL + VST,   // VST
-    B_VREADY = B_VEMPTY + VST,  // VST: V stage converted to fp16
+    B_STEP = B_KFULL + KST,     // 2: all MMAs of key step jj done (by parity of jj); the K and
+                                // V stages that step n reuses are both freed by step n - 2
+    B_VFULL = B_STEP + 2,       // VST
+    B_VREADY = B_VFULL + VST,   // VST: V stage converted to fp16
     B_SFULL = B_VREADY + VST,   // 2 (per tile)
     B_PFULL = B_SFULL + 2,      // 2 (per tile)
     B_OFULL = B_PFULL + 2,      // 2 (per tile)
@@ -231,13 +234,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(&bar[B_Q], 1);
-        for (int s = 0; s < KST; ++s) {
-            mbar_init(&bar[B_KFULL + s], 1);
-            mbar_init(&bar[B_KEMPTY + s], 1);
-        }
+        for (int s = 0; s < KST; ++s) mbar_init(&bar[B_KFULL + s], 1);
+        for (int s = 0; s < 2; ++s) mbar_init(&bar[B_STEP + s], 1);
         for (int s = 0; s < VST; ++s) {
             mbar_init(&bar[B_VFULL + s], 1);
-            mbar_init(&bar[B_VEMPTY + s], 1);
             mbar_init(&bar[B_VREADY + s], 64);
         }
         for (int t = 0; t < 2; ++t) {
@@ -272,15 +272,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             int issued_k[KST] = {}, issued_v[VST] = {};
             for (int jj = 0; jj < nJ; ++jj) {
                 const int j = jb + jj;
+                // K_jj and V_jj reuse the stages of K_jj-2 and V_jj-3, both last read by the
+                // MMAs of step jj - 2
+                if (jj >= 2 &&
+                    !mbar_wait(&bar[B_STEP + ((jj - 2) & 1)], ((jj - 2) >> 1) & 1, abort_flag))
+                    break;
                 const int sk = jj % KST, uk = jj / KST;
-                if (uk > 0 && !mbar_wait(&bar[B_KEMPTY + sk], (uk - 1) & 1, abort_flag)) break;
                 mbar_arrive_expect_tx(&bar[B_KFULL + sk], kTile);
                 for (int x = 0; x < G::NBOX; ++x)
                     tma_load_4d(smem + kOffK + sk * kTile + x * kBox, &tk, &bar[B_KFULL + sk],
                                 x * 64, j * BN, g, b);
                 issued_k[sk] = uk + 1;
                 const int sv = jj % VST, uv = jj / VST;
-                if (uv > 0 && !mbar_wait(&bar[B_VEMPTY + sv], (uv - 1) & 1, abort_flag)) break;
                 mbar_arrive_expect_tx(&bar[B_VFULL + sv], kTile);
                 for (int x = 0; x < G::NBOX; ++x)
                     tma_load_4d(smem + kOffV + sv * kTile + x * kBox, &tv, &bar[B_VFULL + sv],
@@ -347,8 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (!ok) break;
-                if (do_s) mma_commit(&bar[B_KEMPTY + jj % KST]);
-                if (do_pv) mma_commit(&bar[B_VEMPTY + (jj - 1) % VST]);
+                mma_commit(&bar[B_STEP + (jj & 1)]);  // frees K_jj and V_jj-1
             }
             // drain: all issued tcgen05 work finishes before TMEM is released
             mma_commit(&bar[B_DRAIN]);
