@@ -531,18 +531,40 @@ def main():
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdq, hdk, hdv, hdsl))
         d2h = ho.numel() * ho.element_size() + hdo.numel() * hdo.element_size()
 
+        copy_stream = torch.cuda.Stream(device=dev)
+        oo = torch.empty_like(q)
+        od = torch.empty_like(do)
+
         def e2e_step():
-            dq2.copy_(hq, non_blocking=True)
-            dk2.copy_(hk, non_blocking=True)
-            dv2.copy_(hv, non_blocking=True)
-            oo = cga.prefill(dq2, dk2, dv2, causal=True)
-            ho.copy_(oo, non_blocking=True)
-            ddq.copy_(hdq, non_blocking=True)
-            ddk.copy_(hdk, non_blocking=True)
-            ddv.copy_(hdv, non_blocking=True)
-            ddsl.copy_(hdsl, non_blocking=True)
-            od = cga.decode(ddq, ddk, ddv, ddsl)
-            hdo.copy_(od, non_blocking=True)
+            # the step's copies overlap its compute where the data allows: the decode inputs
+            # go up while the prefill runs, the prefill output comes down while decode runs
+            ev_in = torch.cuda.Event()
+            ev_pre = torch.cuda.Event()
+            ev_dec_in = torch.cuda.Event()
+            ev_dec = torch.cuda.Event()
+            copy_stream.wait_stream(stream)  # the previous step is done with every buffer
+            with torch.cuda.stream(copy_stream):
+                dq2.copy_(hq, non_blocking=True)
+                dk2.copy_(hk, non_blocking=True)
+                dv2.copy_(hv, non_blocking=True)
+                ev_in.record(copy_stream)
+                ddq.copy_(hdq, non_blocking=True)
+                ddk.copy_(hdk, non_blocking=True)
+                ddv.copy_(hdv, non_blocking=True)
+                ddsl.copy_(hdsl, non_blocking=True)
+                ev_dec_in.record(copy_stream)
+            stream.wait_event(ev_in)
+            cga.prefill(dq2, dk2, dv2, causal=True, out=oo)
+            ev_pre.record(stream)
+            stream.wait_event(ev_dec_in)
+            cga.decode(ddq, ddk, ddv, ddsl, out=od)
+            ev_dec.record(stream)
+            with torch.cuda.stream(copy_stream):
+                copy_stream.wait_event(ev_pre)
+                ho.copy_(oo, non_blocking=True)
+                copy_stream.wait_event(ev_dec)
+                hdo.copy_(od, non_blocking=True)
+            stream.wait_stream(copy_stream)  # the step ends when its results are on the host
 
         for _ in range(2):
             e2e_step()
