@@ -45,6 +45,10 @@ PREFILL = workloads.CONFIGS["c5b"]
 DECODE = workloads.CONFIGS["c4b"]
 METRIC = "prefill attention TFLOP/s and decode KV-read GB/s, % of GB300 roofline"
 FLUSH_BYTES = 512 << 20
+# Nominal GB300 figures, reported beside the measured peaks: dense bf16 tensor throughput and
+# HBM3e bandwidth ("about 8 TB/s").
+NOMINAL_BF16_TFLOPS = 2250.0
+NOMINAL_HBM_GBS = 8000.0
 DECODE_SETS = 4
 DECODE_CALLS = 16
 
@@ -258,6 +262,39 @@ def oracle_sample(seconds: float):
                    f"{t_dec:.1f} s; fp64, OpenMP over rows"),
         "seconds": t_pref + t_dec,
     }
+
+
+def cpu_model() -> str:
+    """The host CPU's model name, as the OS reports it."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+
+    return platform.processor() or platform.machine()
+
+
+def oracle_single_core():
+    """The fp64 oracle on one core for the three small configured prefill workloads (every
+    causal setting each names), full size: seconds and GFLOP/s."""
+    import oracle
+
+    lib = oracle.load()
+    out = {}
+    for name in ("c1", "c2", "c3"):
+        cfg = workloads.CONFIGS[name]
+        q, k, v = workloads.config_prefill_inputs(cfg)
+        for causal in cfg.causal:
+            t0 = time.perf_counter()
+            oracle.prefill(q, k, v, causal, cfg.scale, nthreads=1, lib=lib)
+            dt = time.perf_counter() - t0
+            fl = workloads.prefill_flops(cfg.B, cfg.Hq, cfg.S, cfg.D, causal)
+            out[f"{name}_{'causal' if causal else 'full'}"] = {"s": dt, "gflops": fl / dt / 1e9}
+    return out
 
 
 def run_reference(args):
@@ -592,7 +629,8 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         r = oracle_sample(args.cpu_seconds)
         cpu = {"value": r["prefill_tflops"], "unit": "TFLOP/s", "cores": r["cores"],
-               "kind": "oracle", "sample": r["sample"], "decode_gbs": r["decode_gbs"]}
+               "kind": "oracle", "sample": r["sample"], "decode_gbs": r["decode_gbs"],
+               "cpu_model": cpu_model(), "single_core": oracle_single_core()}
 
     if args.only != "all":
         if rank == 0:
@@ -619,12 +657,14 @@ def main():
             "config": config_block(),
             "prefill": {"value": tflops, "unit": "TFLOP/s", "ms": pre_mean,
                         "flops": pflops, "frac_of_bf16_peak": tflops / peak_t,
-                        "frac_of_bf16_sustained": tflops / pk["bf16_tflops_sustained"]},
+                        "frac_of_bf16_sustained": tflops / pk["bf16_tflops_sustained"],
+                        "frac_of_nominal": tflops / NOMINAL_BF16_TFLOPS},
             "decode": {"value": dec_gbs, "unit": "GB/s", "ms": dec_mean, "bytes": dec_bytes,
                        "back_to_back": b2b,
                        "roofline": {"bound": "hbm", "achieved": dec_gbs,
                                     "peak": pk["hbm_gbs"], "unit": "GB/s",
                                     "frac": dec_gbs / pk["hbm_gbs"],
+                                    "frac_of_nominal": dec_gbs / NOMINAL_HBM_GBS,
                                     "traffic": traffic["decode_stream_kernel"]
                                     if args.decode_batch is None and args.decode_len is None
                                     else None}},
