@@ -677,7 +677,7 @@ def main():
             "extras": extras,
             "cpu_baseline": cpu,
             "clocks": clocks,
-            "gpu_launches": 3 * args.steps,
+            "gpu_launches": 4 * args.steps,  # V conversion + prefill, decode stream + merge
             "wall_s_timed_region": t_wall,
         }
         print(json.dumps(line), flush=True)

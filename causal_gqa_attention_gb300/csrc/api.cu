@@ -55,10 +55,11 @@ Strides contiguous(int H, long long rows, int D)
     return Strides{(long long)H * rows * D, D, rows * D};
 }
 
-// bf16 tensor viewed as {D, rows, heads, batch} with the given element strides, a 64-column x
-// 128-row box and 128-byte swizzle; reads past `rows` (or any extent) fill with zeros.
+// 16-bit tensor (bf16, or fp16 with f16 = true) viewed as {D, rows, heads, batch} with the
+// given element strides, a 64-column x 128-row box and 128-byte swizzle; reads past `rows` (or
+// any extent) fill with zeros.
 bool encode_bf16_4d(CUtensorMap *m, const void *base, int D, long long rows, int heads, int batch,
-                    const Strides &st)
+                    const Strides &st, bool f16 = false)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
@@ -68,7 +69,8 @@ bool encode_bf16_4d(CUtensorMap *m, const void *base, int D, long long rows, int
                                    (cuuint64_t)st.b * 2};  // bytes, dims 1..3
     const cuuint32_t box[4] = {64, 128, 1, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
+    return fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+              const_cast<void *>(base), dims, strides,
               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -150,6 +152,44 @@ int sm_count(int *out)
     return ATTN_OK;
 }
 
+// Largest fp16 copy of V a prefill call makes in the library-owned scratch; larger calls convert
+// V on chip instead.
+constexpr size_t kMaxV16Bytes = size_t(1) << 30;
+
+// Scratch for one tensor-core prefill call: the key split's partial results (split_bytes; 0 =
+// no split) followed, 256-byte aligned, by the fp16 copy of V (v16_bytes). Sets a.vpre, a.v16,
+// a.ws_o / a.ws_lse and a.J (kept only if its partials fit). If the scratch cannot grow now
+// (stream capture) the call runs without what does not fit: no split, and V converted on chip.
+int prefill_scratch(PrefillTcArgs &a, int J, size_t split_bytes, size_t v16_bytes,
+                    cudaStream_t st)
+{
+    const size_t off = (split_bytes + 255) & ~(size_t)255;
+    const bool want_v16 = v16_bytes <= kMaxV16Bytes;
+    void *ws = nullptr;
+    int rc = ATTN_ERR_WORKSPACE;
+    bool split = J > 0, v16 = want_v16;
+    if (split && v16) rc = workspace_acquire(off + v16_bytes, st, true, &ws);
+    if (rc == ATTN_ERR_WORKSPACE && v16) {
+        split = false;
+        rc = workspace_acquire(v16_bytes, st, true, &ws);
+    }
+    if (rc != ATTN_OK && rc != ATTN_ERR_WORKSPACE) return rc;
+    if (rc == ATTN_ERR_WORKSPACE) split = v16 = false;
+    a.J = 0;
+    a.vpre = 0;
+    if (split) {
+        const size_t blocks = split_bytes / ((size_t)256 * (a.D + 1) * sizeof(float));
+        a.J = J;
+        a.ws_o = static_cast<float *>(ws);
+        a.ws_lse = a.ws_o + blocks * 256 * a.D;
+    }
+    if (v16) {
+        a.vpre = 1;
+        a.v16 = static_cast<uint8_t *>(ws) + (split ? off : 0);
+    }
+    return ATTN_OK;
+}
+
 int check_prefill(const void *q, const void *k, const void *v, void *o, float *lse, int B,
                   int S, int Hq, int Hkv, int D, float scale, int in_t, int out_t)
 {
@@ -213,24 +253,24 @@ int prefill_bf16(const void *q, const void *k, const void *v, void *o, float *ls
     int rc = status_ptr(&a.status);
     if (rc != ATTN_OK) return rc;
     // Small grids (fewer row blocks x heads than SMs) split the keys of each row block over
-    // several blocks and merge; the partials use the library-owned scratch. If that scratch
-    // cannot grow now (stream capture), the unsplit kernel runs instead.
+    // several blocks and merge; the partials use the library-owned scratch, as does the fp16
+    // copy of V.
     int sms = 0;
     rc = sm_count(&sms);
     if (rc != ATTN_OK) return rc;
+    a.sms = sms;
     int J = 0;
     const size_t need = gqa::prefill_split_plan(B, S, Hq, D, causal ? 1 : 0, sms, &J);
-    if (J > 0) {
-        void *ws = nullptr;
-        rc = workspace_acquire(need, st, true, &ws);
-        if (rc == ATTN_OK) {
-            const size_t blocks = need / ((size_t)256 * (D + 1) * sizeof(float));
-            a.J = J;
-            a.ws_o = static_cast<float *>(ws);
-            a.ws_lse = a.ws_o + blocks * 256 * D;
-        } else if (rc != ATTN_ERR_WORKSPACE) {
-            return rc;
-        }
+    rc = prefill_scratch(a, J, need, (size_t)B * Hkv * S * D * 2, st);
+    if (rc != ATTN_OK) return rc;
+    if (a.vpre) {
+        a.v_src = v;
+        a.v_sb = vs.b;
+        a.v_ss = vs.s;
+        a.v_sh = vs.h;
+        a.v_rows = S;
+        if (!encode_bf16_4d(&a.tv, a.v16, D, S, Hkv, B, contiguous(Hkv, S, D), true))
+            return ATTN_ERR_CUDA;
     }
     return cuda_status(gqa::launch_prefill_tc(a, out_dtype == ATTN_F32, st));
 }
@@ -356,6 +396,22 @@ int chunk_or_varlen(const void *q, const void *kcache, const void *vcache, const
     a.front = front;
     rc = status_ptr(&a.status);
     if (rc != ATTN_OK) return rc;
+    int sms = 0;
+    rc = sm_count(&sms);
+    if (rc != ATTN_OK) return rc;
+    a.sms = sms;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    rc = prefill_scratch(a, 0, 0, (size_t)B * Hkv * max_len * D * 2, st);
+    if (rc != ATTN_OK) return rc;
+    if (a.vpre) {
+        const Strides cs = contiguous(Hkv, max_len, D);
+        a.v_src = vcache;
+        a.v_sb = cs.b;
+        a.v_ss = cs.s;
+        a.v_sh = cs.h;
+        a.v_rows = max_len;
+        if (!encode_bf16_4d(&a.tv, a.v16, D, max_len, Hkv, B, cs, true)) return ATTN_ERR_CUDA;
+    }
     return cuda_status(gqa::launch_prefill_tc(a, out_dtype == ATTN_F32,
                                               static_cast<cudaStream_t>(stream)));
 }

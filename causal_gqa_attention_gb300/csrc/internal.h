@@ -31,6 +31,15 @@ struct PrefillTcArgs {
     int J = 0;
     float *ws_o = nullptr;    // [blocks, 256, D] fp32
     float *ws_lse = nullptr;  // [blocks, 256] fp32
+    // vpre != 0: V is first converted to a contiguous fp16 copy v16 [B, Hkv, v_rows, D] (from
+    // v_src, element (b, g, r, d) at v_src + b v_sb + r v_ss + g v_sh + d) and tv maps that copy
+    // as fp16; vpre == 0: tv maps the bf16 V and the kernel converts on chip. Required with J.
+    int vpre = 0;
+    const void *v_src = nullptr;
+    long long v_sb = 0, v_ss = 0, v_sh = 0;
+    void *v16 = nullptr;
+    int v_rows = 0;
+    int sms = 0;  // SM count (sizes the conversion grid)
 };
 cudaError_t launch_prefill_tc(const PrefillTcArgs &a, bool out_f32, cudaStream_t stream);
 // Chooses the key split for a prefill shape on num_sms SMs: writes J (0 = no split) and returns

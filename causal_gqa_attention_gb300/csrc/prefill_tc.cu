@@ -5,16 +5,20 @@
 //
 // One thread block owns 256 consecutive query rows of one (batch, query head): two 128-row
 // Q tiles (HD = 128; half as wide at 64). Both tiles consume the same stream of 128-key K/V
-// tiles, so every K/V tile brought in by TMA feeds four tensor-core products. Roles (12 warps):
+// tiles, so every K/V tile brought in by TMA feeds four tensor-core products. Roles (12 warps;
+// 10 when V comes pre-converted, see below):
 //   warp 0      TMA producer: Q tiles once, then K_j into a 2-stage and V_j into a 3-stage ring
 //               (V also waits for its conversion, so it gets one stage more);
-//   warp 1      tcgen05 issuer (one thread): S_t = Q_t K_j^T into TMEM, O_t += P_t V_j with
-//               P_t read from TMEM; owns the TMEM allocation;
-//   warps 2-3   convert each landed V tile from bf16 to fp16 in place (see below);
-//   warps 4-7   softmax for tile 0, warps 8-11 for tile 1: one thread per query row (its TMEM
-//               lane). Reads the 128 scores of its row, masks, updates the running max and
-//               sum, writes P (fp16) over the scores it came from, rescales its O row when
-//               the max moved, and finally writes O / l and the LSE.
+//   warp 1      tcgen05 issuer (the warp runs converged, one elected lane issues each MMA):
+//               S_t = Q_t K_j^T into TMEM, O_t += P_t V_j with P_t read from TMEM; owns the
+//               TMEM allocation;
+//   warps 2-3   convert each landed V tile from bf16 to fp16 in place (see below), unless
+//               V was converted beforehand;
+//   warps 4-7   softmax for tile 0, warps 8-11 for tile 1 (2-5 and 6-9 with pre-converted V):
+//               one thread per query row (its TMEM lane). Reads the 128 scores of its row,
+//               masks, updates the running max and sum, writes P (fp16) over the scores it
+//               came from, rescales its O row when the max moved, and finally writes O / l
+//               and the LSE.
 // TMEM (512 columns): S_0 | S_1 | O_0 | O_1, 128 fp32 columns each (O uses HD of them); P_t is
 // packed fp16 in the first 64 columns of S_t. S and P never leave the SM.
 //
@@ -22,7 +26,14 @@
 // it. With bf16 (8-bit significand) a peaky softmax (a few keys carrying most of the weight)
 // showed errors near 8e-3 in the output; fp16 (11-bit significand) brings that to about 1e-3.
 // The tensor core needs both operands of one product in the same type, so V is converted to
-// fp16 in shared memory; that is exact for every bf16 value with 2^-14 <= |v| <= 65280.
+// fp16; that is exact for every bf16 value with 2^-14 <= |v| <= 65280. Normally a separate
+// HBM-bound kernel (convert_v_kernel) writes an fp16 copy of V once per call and the attention
+// kernel streams that: every V tile is read by many blocks (all heads of its group, all later
+// row blocks), and converting it in shared memory in each of them cost more than the copy. The
+// conversion also competed with the scores MMAs for shared-memory bandwidth (the tensor core
+// wins), which made it the slowest stage of the pipeline. When no scratch is available for the
+// copy (stream capture before the scratch has grown) warps 2-3 convert each landed tile in
+// place instead; both ways give the same fp16 values.
 //
 // The two tiles alternate on the tensor core: while tile 0's softmax runs, the tensor core
 // computes tile 1's P V and next S, and the other way round. Issue order per key tile j:
@@ -58,7 +69,9 @@ namespace {
 
 constexpr int BM = 128;        // query rows per tile = TMEM lanes
 constexpr int BN = 128;        // keys per K/V tile
-constexpr int kThreads = 384;  // 12 warps
+// 12 warps when the kernel converts V itself, 10 when V arrives converted (no converter warps)
+template <bool VPRE>
+constexpr int kThreads = VPRE ? 320 : 384;
 constexpr uint32_t kBox = 16384;          // one 128-row x 64-col bf16 box (128-byte rows)
 constexpr int KST = 2;                    // K ring stages
 constexpr int VST = 3;                    // V ring stages (V also waits for its fp16 conversion)
@@ -66,6 +79,10 @@ constexpr int VST = 3;                    // V ring stages (V also waits for its
 // the P V of step jj - 2): one "step jj - 2 done" barrier covers both.
 static_assert(KST == 2 && VST == 3, "stage reuse tied to step jj - 2");
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
+#ifndef PREFILL_PREFETCH
+#define PREFILL_PREFETCH 2
+#endif
+constexpr int kPrefetch = PREFILL_PREFETCH;       // L2 prefetch distance in key tiles
 
 // Shared-memory plan for head dim HD (64 or 128): two Q tiles, the K ring, the V ring, then the
 // barriers. A tile is 128 rows x HD bf16, stored as HD / 64 boxes of 64 columns.
@@ -164,8 +181,10 @@ __device__ __noinline__ void zero_v_tail(uint4 *tile, int ct, int rows_ok, int n
 // SPLIT = true: one block per (row block, key segment of J tiles, head, batch); it writes the
 // segment's normalised O (fp32) and its LSE (log2 units) to ws_o / ws_lse, and
 // prefill_split_merge_kernel combines the segments of each row.
-template <int HD, bool OUT_F32, bool SPLIT>
-__global__ void __launch_bounds__(kThreads, 1)
+// VPRE = true: tv maps an fp16 copy of V written by convert_v_kernel (no converter warps; the
+// softmax warps are 2-9). VPRE = false: tv maps the bf16 V, converted on chip by warps 2-3.
+template <int HD, bool OUT_F32, bool SPLIT, bool VPRE>
+__global__ void __launch_bounds__(kThreads<VPRE>, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, void *__restrict__ out,
                       float *__restrict__ lse, int B, int S, int Hq, int Hkv, float scale_log2,
@@ -184,6 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    constexpr int kSoftmaxWarp0 = VPRE ? 2 : 4;  // first of the 8 softmax warps
 
     // ---- work item: heaviest row blocks first (causal), heads of one group adjacent
     const int n_rb = (S + 2 * BM - 1) / (2 * BM);
@@ -289,6 +309,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_4d(smem + kOffV + sv * kTile + x * kBox, &tv, &bar[B_VFULL + sv],
                                 x * 64, j * BN, g, b);
                 issued_v[sv] = uv + 1;
+                // the K/V tiles kPrefetch steps ahead go to L2 now: their stages free up only
+                // about one step before they are needed, less than a DRAM round trip under load
+                if (kPrefetch > 0 && jj + kPrefetch < nJ)
+                    for (int x = 0; x < G::NBOX; ++x) {
+                        tma_prefetch_l2_4d(&tk, x * 64, (j + kPrefetch) * BN, g, b);
+                        tma_prefetch_l2_4d(&tv, x * 64, (j + kPrefetch) * BN, g, b);
+                    }
             }
             if (*abort_flag) {
                 // let every copy this block started land before the block exits
@@ -302,62 +329,65 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ================================================================ tcgen05 issuer
-        if (lane == 0) {
-            constexpr uint32_t idS = idesc_f32acc(BM, BN, 0, 0, 1);  // bf16 Q, K: K-major
-            constexpr uint32_t idO = idesc_f32acc(BM, HD, 0, 1, 0);  // fp16 P (TMEM), V MN-major
-            const uint32_t sQ = smem_u32(smem + kOffQ);
-            const uint32_t sK = smem_u32(smem + kOffK);
-            const uint32_t sV = smem_u32(smem + kOffV);
-            bool ok = mbar_wait(&bar[B_Q], 0, abort_flag);
-            for (int jj = 0; ok && jj <= nJ; ++jj) {
-                const int j = jb + jj;
-                const bool do_s = jj < nJ;
-                const bool do_pv = jj >= 1;
-                if (do_s && !mbar_wait(&bar[B_KFULL + jj % KST], (jj / KST) & 1, abort_flag)) break;
-                if (do_pv &&
-                    !mbar_wait(&bar[B_VREADY + (jj - 1) % VST], ((jj - 1) / VST) & 1, abort_flag))
-                    break;
-                tc_fence_after();
-                for (int t = 0; t < 2 && ok; ++t) {
-                    if (do_pv && j - 1 <= hi[t]) {
-                        if (!mbar_wait(&bar[B_PFULL + t], (jj - 1) & 1, abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t vbase = sV + ((jj - 1) % VST) * kTile;
-#pragma unroll
-                        for (int kk = 0; kk < BN / 16; ++kk) {
-                            // B = V rows 16kk..16kk+15: MN-major, 64-col chunks 16 KB apart
-                            // (one chunk when HD = 64), 8-row groups 1 KB apart
-                            const uint64_t bd = smem_desc_sw128(vbase + kk * 2048, kBox, 1024);
-                            mma_ts(tmem + kColO + t * 128, tmem + kColS + t * 128 + kk * 8, bd,
-                                   idO, (jj - 1 > 0 || kk > 0) ? 1u : 0u);
-                        }
-                        if (j - 1 == hi[t]) mma_commit(&bar[B_OFULL + t]);
+        // The whole warp runs this loop converged; one elected lane issues each MMA and commit.
+        constexpr unsigned FULL = 0xffffffffu;
+        constexpr uint32_t idS = idesc_f32acc(BM, BN, 0, 0, 1);  // bf16 Q, K: K-major
+        constexpr uint32_t idO = idesc_f32acc(BM, HD, 0, 1, 0);  // fp16 P (TMEM), V MN-major
+        const uint32_t sQ = smem_u32(smem + kOffQ);
+        const uint32_t sK = smem_u32(smem + kOffK);
+        const uint32_t sV = smem_u32(smem + kOffV);
+        bool ok = __all_sync(FULL, mbar_wait(&bar[B_Q], 0, abort_flag));
+        for (int jj = 0; ok && jj <= nJ; ++jj) {
+            const int j = jb + jj;
+            const bool do_s = jj < nJ;
+            const bool do_pv = jj >= 1;
+            if (do_s &&
+                !__all_sync(FULL, mbar_wait(&bar[B_KFULL + jj % KST], (jj / KST) & 1, abort_flag)))
+                break;
+            if (do_pv && !__all_sync(FULL, mbar_wait(&bar[(VPRE ? B_VFULL : B_VREADY) + (jj - 1) % VST],
+                                                     ((jj - 1) / VST) & 1, abort_flag)))
+                break;
+            tc_fence_after();
+            for (int t = 0; t < 2 && ok; ++t) {
+                if (do_pv && j - 1 <= hi[t]) {
+                    if (!__all_sync(FULL, mbar_wait(&bar[B_PFULL + t], (jj - 1) & 1, abort_flag))) {
+                        ok = false;
+                        break;
                     }
-                    if (do_s && j <= hi[t]) {
-                        const uint32_t qbase = sQ + t * kTile;
-                        const uint32_t kbase = sK + (jj % KST) * kTile;
+                    tc_fence_after();
+                    const uint32_t vbase = sV + ((jj - 1) % VST) * kTile;
 #pragma unroll
-                        for (int kk = 0; kk < HD / 16; ++kk) {
-                            const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-                            const uint64_t ad = smem_desc_sw128(qbase + off, 16, 1024);
-                            const uint64_t bd = smem_desc_sw128(kbase + off, 16, 1024);
-                            mma_ss(tmem + kColS + t * 128, ad, bd, idS, kk > 0 ? 1u : 0u);
-                        }
-                        mma_commit(&bar[B_SFULL + t]);
+                    for (int kk = 0; kk < BN / 16; ++kk) {
+                        // B = V rows 16kk..16kk+15: MN-major, 64-col chunks 16 KB apart (one
+                        // chunk when HD = 64), 8-row groups 1 KB apart
+                        const uint64_t bd = smem_desc_sw128(vbase + kk * 2048, kBox, 1024);
+                        mma_ts_warp(tmem + kColO + t * 128, tmem + kColS + t * 128 + kk * 8, bd,
+                                    idO, (jj - 1 > 0 || kk > 0) ? 1u : 0u);
                     }
+                    if (j - 1 == hi[t]) mma_commit_warp(&bar[B_OFULL + t]);
                 }
-                if (!ok) break;
-                mma_commit(&bar[B_STEP + (jj & 1)]);  // frees K_jj and V_jj-1
+                if (do_s && j <= hi[t]) {
+                    const uint32_t qbase = sQ + t * kTile;
+                    const uint32_t kbase = sK + (jj % KST) * kTile;
+#pragma unroll
+                    for (int kk = 0; kk < HD / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+                        const uint64_t ad = smem_desc_sw128(qbase + off, 16, 1024);
+                        const uint64_t bd = smem_desc_sw128(kbase + off, 16, 1024);
+                        mma_ss_warp(tmem + kColS + t * 128, ad, bd, idS, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit_warp(&bar[B_SFULL + t]);
+                }
             }
-            // drain: all issued tcgen05 work finishes before TMEM is released
-            mma_commit(&bar[B_DRAIN]);
-            volatile int never = 0;
-            mbar_wait(&bar[B_DRAIN], 0, &never);
+            if (!ok) break;
+            mma_commit_warp(&bar[B_STEP + (jj & 1)]);  // frees K_jj and V_jj-1
         }
-    } else if (warp == 2 || warp == 3) {
+        // drain: all issued tcgen05 work finishes before TMEM is released
+        mma_commit_warp(&bar[B_DRAIN]);
+        volatile int never = 0;
+        mbar_wait(&bar[B_DRAIN], 0, &never);
+        __syncwarp();
+    } else if (!VPRE && (warp == 2 || warp == 3)) {
         // ================================================================ V bf16 -> fp16
         // The P V product runs in fp16 (10-bit mantissa for P instead of bf16's 7): each V tile
         // is converted in place once it lands, then handed to the tensor core.
@@ -389,9 +419,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&bar[B_VREADY + s]);
         }
         if (over) atomicOr(status, 4u);
-    } else if (warp >= 4) {
+    } else if (warp >= kSoftmaxWarp0) {
         // ================================================================ softmax / epilogue
-        const int t = (warp - 4) / 4;
+        const int t = (warp - kSoftmaxWarp0) / 4;
         const int wq = warp & 3;
         const int r = wq * 32 + lane;  // row within the tile = TMEM lane
         const int i = q0 + t * BM + r;  // query row
@@ -645,7 +675,73 @@ __global__ void __launch_bounds__(256)
         lse[orow] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
 }
 
-template <int HD, bool OUT_F32, bool SPLIT>
+// V (bf16, element (b, g, r, d) at v + b sb + r ss + g sh + d) -> a contiguous fp16 copy
+// [B, Hkv, rows, HD] for the P V product, saturating like the on-chip conversion (status bit 4
+// when a value does not fit). With kv_lens, rows at or past a sequence's key count are written
+// as 0 up to the end of their 128-row key tile (the attention kernel reads whole tiles, and
+// 0 * NaN from a stale cache row would not be 0); later tiles are never read and are skipped.
+// Grid: x blocks stride over one (b, g) slab, y over the slabs.
+template <int HD>
+__global__ void __launch_bounds__(256)
+    convert_v_kernel(const __nv_bfloat16 *__restrict__ v, long long sb, long long ss,
+                     long long sh, uint4 *__restrict__ v16, int B, int Hkv, int rows,
+                     const int *__restrict__ kv_lens, int max_kv, unsigned *__restrict__ status)
+{
+    constexpr int CPR = HD / 8;  // 16-byte chunks per row
+    constexpr int LOG = HD == 128 ? 4 : 3;
+    uint32_t over = 0;
+    const int nbg = B * Hkv;
+    for (int bg = blockIdx.y; bg < nbg; bg += gridDim.y) {
+        const int b = bg / Hkv, g = bg - b * Hkv;
+        int L = rows;
+        if (kv_lens != nullptr) {
+            L = kv_lens[b];
+            L = L < 0 ? 0 : (L > max_kv ? max_kv : L);
+        }
+        const long long lim = (long long)min((L + 127) & ~127, rows) * CPR;
+        const __nv_bfloat16 *src = v + b * sb + g * sh;
+        uint4 *dst = v16 + (long long)bg * rows * CPR;
+        for (long long i = blockIdx.x * 256LL + threadIdx.x; i < lim;
+             i += (long long)gridDim.x * 256) {
+            const long long r = i >> LOG;
+            const int c = (int)(i & (CPR - 1));
+            uint4 w = make_uint4(0, 0, 0, 0);
+            if (r < L) {
+                w = *reinterpret_cast<const uint4 *>(src + r * ss + c * 8);
+                over |= too_big_for_f16(w.x) | too_big_for_f16(w.y) | too_big_for_f16(w.z) |
+                        too_big_for_f16(w.w);
+                w.x = bf16x2_to_f16x2_sat(w.x);
+                w.y = bf16x2_to_f16x2_sat(w.y);
+                w.z = bf16x2_to_f16x2_sat(w.z);
+                w.w = bf16x2_to_f16x2_sat(w.w);
+            }
+            dst[i] = w;
+        }
+    }
+    if (__any_sync(0xffffffffu, over != 0) && (threadIdx.x & 31) == 0) atomicOr(status, 4u);
+}
+
+cudaError_t launch_convert_v(const PrefillTcArgs &a, cudaStream_t st)
+{
+    const int nbg = a.B * a.Hkv;
+    const int y = nbg < 65535 ? nbg : 65535;
+    const long long per = ((long long)a.v_rows * (a.D / 8) + 255) / 256;  // blocks per slab
+    long long x = (8LL * a.sms + y - 1) / y;  // about 8 blocks of 256 threads per SM in all
+    if (x > per) x = per;
+    if (x < 1) x = 1;
+    const dim3 grid((unsigned)x, (unsigned)y);
+    const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(a.v_src);
+    uint4 *dst = static_cast<uint4 *>(a.v16);
+    if (a.D == 128)
+        convert_v_kernel<128><<<grid, 256, 0, st>>>(src, a.v_sb, a.v_ss, a.v_sh, dst, a.B, a.Hkv,
+                                                    a.v_rows, a.kv_lens, a.max_kv, a.status);
+    else
+        convert_v_kernel<64><<<grid, 256, 0, st>>>(src, a.v_sb, a.v_ss, a.v_sh, dst, a.B, a.Hkv,
+                                                   a.v_rows, a.kv_lens, a.max_kv, a.status);
+    return cudaGetLastError();
+}
+
+template <int HD, bool OUT_F32, bool SPLIT, bool VPRE>
 cudaError_t launch_t(const PrefillTcArgs &a, cudaStream_t st)
 {
     static bool attr_set[64] = {};  // the attribute is set once per device
@@ -653,7 +749,7 @@ cudaError_t launch_t(const PrefillTcArgs &a, cudaStream_t st)
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 64 || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(prefill_tc_kernel<HD, OUT_F32, SPLIT>,
+        e = cudaFuncSetAttribute(prefill_tc_kernel<HD, OUT_F32, SPLIT, VPRE>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<HD>::kSmem);
         if (e != cudaSuccess) return e;
         if (dev < 64) attr_set[dev] = true;
@@ -662,7 +758,11 @@ cudaError_t launch_t(const PrefillTcArgs &a, cudaStream_t st)
     long long blocks = (long long)n_rb * a.Hq * a.B;
     const int NS = SPLIT ? split_slots(a.S, a.causal, a.J) : 1;
     if (SPLIT) blocks = (long long)n_rb * NS * a.Hq * a.B;
-    prefill_tc_kernel<HD, OUT_F32, SPLIT><<<(unsigned)blocks, kThreads, Geo<HD>::kSmem, st>>>(
+    if (VPRE) {
+        e = launch_convert_v(a, st);
+        if (e != cudaSuccess) return e;
+    }
+    prefill_tc_kernel<HD, OUT_F32, SPLIT, VPRE><<<(unsigned)blocks, kThreads<VPRE>, Geo<HD>::kSmem, st>>>(
         a.tq, a.tk, a.tv, a.o, a.lse, a.B, a.S, a.Hq, a.Hkv, a.scale_log2, a.causal, a.status,
         a.J, a.ws_o, a.ws_lse, a.kv_lens, a.kv_lens ? a.max_kv : a.S, a.front, a.o_sb, a.o_ss,
         a.o_sh, NS);
@@ -686,9 +786,14 @@ cudaError_t launch_t(const PrefillTcArgs &a, cudaStream_t st)
 template <int HD>
 cudaError_t launch_hd(const PrefillTcArgs &a, bool out_f32, cudaStream_t st)
 {
+    // the key split always has scratch, so it always has the fp16 copy of V as well
     if (a.J > 0)
-        return out_f32 ? launch_t<HD, true, true>(a, st) : launch_t<HD, false, true>(a, st);
-    return out_f32 ? launch_t<HD, true, false>(a, st) : launch_t<HD, false, false>(a, st);
+        return out_f32 ? launch_t<HD, true, true, true>(a, st)
+                       : launch_t<HD, false, true, true>(a, st);
+    if (a.vpre)
+        return out_f32 ? launch_t<HD, true, false, true>(a, st)
+                       : launch_t<HD, false, false, true>(a, st);
+    return out_f32 ? launch_t<HD, true, false, false>(a, st) : launch_t<HD, false, false, false>(a, st);
 }
 
 }  // namespace

@@ -117,6 +117,16 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// 4-D tiled prefetch of a box into L2 (no shared memory, no completion signal): a later
+// tma_load_4d of the same box then waits on L2 instead of DRAM.
+__device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap *map, int x, int y, int z, int w)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z), "r"(w)
+                 : "memory");
+}
+
 // 1-D bulk copy global -> shared (size and both addresses multiples of 16 bytes), completion
 // counted in bytes on `bar`.
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
@@ -181,6 +191,43 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar)
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_u32(bar))
         : "memory");
+}
+
+// The same three operations issued by a converged warp: every lane executes the statement and
+// the one lane picked by elect.sync issues. Measured on sm_103a with the scores / P V issue
+// pattern of the prefill kernel (alternating batches of 8 MMAs, commits between them): about
+// 66 cycles per 128x128x16 MMA (the tensor core's rate) this way, 77 when a lone active thread
+// issues, because that thread spends about as long issuing each MMA as the tensor core takes
+// to execute it and falls behind on the barrier work in between.
+__device__ __forceinline__ void mma_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p, e;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "elect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p, e;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "elect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_warp(uint64_t *bar)
+{
+    asm volatile("{\n\t.reg .pred e;\n\t"
+                 "elect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
+                 ::"r"(smem_u32(bar))
+                 : "memory");
 }
 
 // Shared-memory matrix descriptor: start address, leading/stride byte offsets, 128-byte swizzle.

@@ -104,3 +104,34 @@ def test_chunk_length_above_cache_is_clamped_and_flagged():
     o_ref, _ = oracle.chunk(q, kc, vc, torch.tensor([256, 256], dtype=torch.int32),
                             1 / math.sqrt(128), True)
     check_out(o, o_ref, "bf16_pre", "clamped chunk")
+
+
+def test_chunk_cache_above_copy_limit_converts_on_chip():
+    """Caches whose fp16 copy of V would exceed the library's 1 GiB limit (B64 Hkv8, 8320 rows of
+    D128): the attention kernel converts V on chip instead. Only the rows below each length are
+    written; the rest of both caches is uninitialised device memory, which must not leak in."""
+    dev = device()
+    B, Hq, Hkv, Sq, max_len = 64, 8, 8, 64, 8320
+    assert B * Hkv * max_len * 128 * 2 > (1 << 30)
+    g = torch.Generator().manual_seed(31)
+    lens = torch.randint(1, 300, (B,), generator=g, dtype=torch.int32)
+    lens[0] = 299
+    lens[1] = 1
+    kc = torch.empty((B, Hkv, max_len, 128), dtype=torch.bfloat16, device=dev)
+    vc = torch.empty_like(kc)
+    kh = torch.randn((B, Hkv, 300, 128), generator=g).to(torch.bfloat16)
+    vh = torch.randn((B, Hkv, 300, 128), generator=g).to(torch.bfloat16)
+    for b in range(B):
+        L = int(lens[b])
+        kc[b, :, :L] = kh[b, :, :L].to(dev)
+        vc[b, :, :L] = vh[b, :, :L].to(dev)
+    q = torch.randn((B, Hq, Sq, 128), generator=g).to(torch.bfloat16)
+    cga = library()
+    o, lse = cga.chunk(q.to(dev), kc, vc, lens.to(dev), causal=True, out_dtype=torch.float32,
+                       return_lse=True)
+    torch.cuda.synchronize()
+    assert cga.device_status() == 0
+    # the oracle sees the written rows only (every length is below 300)
+    o_ref, lse_ref = oracle.chunk(q, kh, vh, lens, 1 / math.sqrt(128), True)
+    check_out(o, o_ref, "bf16_pre", "large-cache chunk")
+    check_lse(lse, lse_ref, "large-cache chunk lse")

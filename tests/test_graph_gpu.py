@@ -103,3 +103,30 @@ def test_chunk_and_varlen_graph_replay():
     torch.cuda.synchronize()
     assert torch.equal(ov, cga.prefill_varlen(qv, kv, vv, lens))
     assert cga.device_status() == 0
+
+
+def test_prefill_captured_before_scratch_grows_matches_eager():
+    """A prefill captured with no warm-up, larger than any scratch the process has grown so far
+    (V of B8 Hkv8 S8192 D128: 134 MB as fp16): the captured call cannot grow the scratch, so it
+    converts V on chip; the eager call afterwards grows it and takes the fp16 copy. Both give
+    the same bits."""
+    cga = library()
+    dev = device()
+    B, Hq, Hkv, S, D = 8, 8, 8, 8192, 128
+    g = torch.Generator(device=dev).manual_seed(12)
+    q = torch.randn((B, Hq, S, D), generator=g, device=dev).to(torch.bfloat16)
+    k = torch.randn((B, Hkv, S, D), generator=g, device=dev).to(torch.bfloat16)
+    v = torch.randn((B, Hkv, S, D), generator=g, device=dev).to(torch.bfloat16)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device=dev)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        cga.prefill(q, k, v, causal=True, out=o, lse=lse, return_lse=True)
+    graph.replay()
+    torch.cuda.synchronize()
+    oe, le = cga.prefill(q, k, v, causal=True, return_lse=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o, oe) and torch.equal(lse, le)
+    assert cga.device_status() == 0
