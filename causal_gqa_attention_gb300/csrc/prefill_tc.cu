@@ -79,10 +79,6 @@ constexpr int VST = 3;                    // V ring stages (V also waits for its
 // the P V of step jj - 2): one "step jj - 2 done" barrier covers both.
 static_assert(KST == 2 && VST == 3, "stage reuse tied to step jj - 2");
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
-#ifndef PREFILL_PREFETCH
-#define PREFILL_PREFETCH 2
-#endif
-constexpr int kPrefetch = PREFILL_PREFETCH;       // L2 prefetch distance in key tiles
 
 // Shared-memory plan for head dim HD (64 or 128): two Q tiles, the K ring, the V ring, then the
 // barriers. A tile is 128 rows x HD bf16, stored as HD / 64 boxes of 64 columns.
@@ -303,19 +299,16 @@ __global__ void __launch_bounds__(kThreads<VPRE>, 1)
                     tma_load_4d(smem + kOffK + sk * kTile + x * kBox, &tk, &bar[B_KFULL + sk],
                                 x * 64, j * BN, g, b);
                 issued_k[sk] = uk + 1;
+                // the fp16 copy of V comes from the conversion kernel just before this one,
+                // which lets this grid start early (programmatic dependent launch): everything
+                // up to here overlaps its tail
+                if (VPRE && jj == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
                 const int sv = jj % VST, uv = jj / VST;
                 mbar_arrive_expect_tx(&bar[B_VFULL + sv], kTile);
                 for (int x = 0; x < G::NBOX; ++x)
                     tma_load_4d(smem + kOffV + sv * kTile + x * kBox, &tv, &bar[B_VFULL + sv],
                                 x * 64, j * BN, g, b);
                 issued_v[sv] = uv + 1;
-                // the K/V tiles kPrefetch steps ahead go to L2 now: their stages free up only
-                // about one step before they are needed, less than a DRAM round trip under load
-                if (kPrefetch > 0 && jj + kPrefetch < nJ)
-                    for (int x = 0; x < G::NBOX; ++x) {
-                        tma_prefetch_l2_4d(&tk, x * 64, (j + kPrefetch) * BN, g, b);
-                        tma_prefetch_l2_4d(&tv, x * 64, (j + kPrefetch) * BN, g, b);
-                    }
             }
             if (*abort_flag) {
                 // let every copy this block started land before the block exits
@@ -344,8 +337,9 @@ __global__ void __launch_bounds__(kThreads<VPRE>, 1)
             if (do_s &&
                 !__all_sync(FULL, mbar_wait(&bar[B_KFULL + jj % KST], (jj / KST) & 1, abort_flag)))
                 break;
-            if (do_pv && !__all_sync(FULL, mbar_wait(&bar[(VPRE ? B_VFULL : B_VREADY) + (jj - 1) % VST],
-                                                     ((jj - 1) / VST) & 1, abort_flag)))
+            const int vbar = (VPRE ? B_VFULL : B_VREADY) + (jj - 1) % VST;  // V_jj-1 usable
+            if (do_pv &&
+                !__all_sync(FULL, mbar_wait(&bar[vbar], ((jj - 1) / VST) & 1, abort_flag)))
                 break;
             tc_fence_after();
             for (int t = 0; t < 2 && ok; ++t) {
@@ -689,6 +683,7 @@ __global__ void __launch_bounds__(256)
 {
     constexpr int CPR = HD / 8;  // 16-byte chunks per row
     constexpr int LOG = HD == 128 ? 4 : 3;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     uint32_t over = 0;
     const int nbg = B * Hkv;
     for (int bg = blockIdx.y; bg < nbg; bg += gridDim.y) {
@@ -758,25 +753,34 @@ cudaError_t launch_t(const PrefillTcArgs &a, cudaStream_t st)
     long long blocks = (long long)n_rb * a.Hq * a.B;
     const int NS = SPLIT ? split_slots(a.S, a.causal, a.J) : 1;
     if (SPLIT) blocks = (long long)n_rb * NS * a.Hq * a.B;
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
     if (VPRE) {
         e = launch_convert_v(a, st);
         if (e != cudaSuccess) return e;
     }
-    prefill_tc_kernel<HD, OUT_F32, SPLIT, VPRE><<<(unsigned)blocks, kThreads<VPRE>, Geo<HD>::kSmem, st>>>(
-        a.tq, a.tk, a.tv, a.o, a.lse, a.B, a.S, a.Hq, a.Hkv, a.scale_log2, a.causal, a.status,
-        a.J, a.ws_o, a.ws_lse, a.kv_lens, a.kv_lens ? a.max_kv : a.S, a.front, a.o_sb, a.o_ss,
-        a.o_sh, NS);
-    e = cudaGetLastError();
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)blocks);
+        cfg.blockDim = dim3(kThreads<VPRE>);
+        cfg.dynamicSmemBytes = Geo<HD>::kSmem;
+        cfg.stream = st;
+        cfg.attrs = pdl;
+        cfg.numAttrs = VPRE ? 1 : 0;  // starts while the conversion kernel finishes
+        e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<HD, OUT_F32, SPLIT, VPRE>, a.tq, a.tk,
+                               a.tv, a.o, a.lse, a.B, a.S, a.Hq, a.Hkv, a.scale_log2, a.causal,
+                               a.status, a.J, a.ws_o, a.ws_lse, a.kv_lens,
+                               a.kv_lens ? a.max_kv : a.S, a.front, a.o_sb, a.o_ss, a.o_sh, NS);
+    }
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess || !SPLIT) return e;
     const long long rows = (long long)a.B * a.Hq * a.S;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((rows + 7) / 8));
     cfg.blockDim = dim3(256);
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
+    cfg.attrs = pdl;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, prefill_split_merge_kernel<HD, OUT_F32>, (const float *)a.ws_o,
                               (const float *)a.ws_lse, a.o, a.lse, a.B, a.S, a.Hq, a.causal, a.J,
@@ -793,7 +797,8 @@ cudaError_t launch_hd(const PrefillTcArgs &a, bool out_f32, cudaStream_t st)
     if (a.vpre)
         return out_f32 ? launch_t<HD, true, false, true>(a, st)
                        : launch_t<HD, false, false, true>(a, st);
-    return out_f32 ? launch_t<HD, true, false, false>(a, st) : launch_t<HD, false, false, false>(a, st);
+    return out_f32 ? launch_t<HD, true, false, false>(a, st)
+                   : launch_t<HD, false, false, false>(a, st);
 }
 
 }  // namespace

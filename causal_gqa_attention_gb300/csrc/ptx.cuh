@@ -117,16 +117,6 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
-// 4-D tiled prefetch of a box into L2 (no shared memory, no completion signal): a later
-// tma_load_4d of the same box then waits on L2 instead of DRAM.
-__device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap *map, int x, int y, int z, int w)
-{
-    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(x), "r"(y), "r"(z), "r"(w)
-                 : "memory");
-}
-
 // 1-D bulk copy global -> shared (size and both addresses multiples of 16 bytes), completion
 // counted in bytes on `bar`.
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)

@@ -74,11 +74,17 @@ typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype;
  * Requires Hq % Hkv == 0, D in {64, 128}, 16-byte aligned pointers.
  * When the shape has fewer (256-row block, head) tiles than the GPU has SMs, the key range of
  * each row block is split over several thread blocks and a second kernel merges their results
- * by log-sum-exp weights; the partial results use the library-owned scratch buffer (grown with
- * cudaMalloc on first use, outside stream capture; during capture the unsplit kernel runs).
+ * by log-sum-exp weights.
  * Computes on tcgen05 tensor cores with fp32 accumulation and fp32 softmax state: Q K^T from
- * the bf16 inputs; P V with P rounded to fp16 and V converted bf16 -> fp16 on chip (exact for
+ * the bf16 inputs; P V with P rounded to fp16 and V converted bf16 -> fp16 (exact for
  * 2^-14 <= |v| <= 65280; larger |v| saturate and set ATTN_DEV_FP16_RANGE in the status word).
+ * The conversion normally writes an fp16 copy of V (B*Hkv*S*D*2 bytes) once per call, which
+ * the attention kernel then streams.
+ * Scratch: the split's partial results and the fp16 copy of V use the library-owned scratch
+ * buffer of the device (grown with cudaMalloc on first use, outside stream capture; the
+ * buffer is shared with the decode calls, so calls on different streams must be serialised).
+ * A call that cannot have the scratch (stream capture before it has grown; a copy above 1 GiB)
+ * runs unsplit and converts V on chip instead, with the same results.
  */
 int attn_prefill(const void *q, const void *k, const void *v, void *o, float *lse, int B, int S,
                  int Hq, int Hkv, int D, float scale, int causal, void *stream);
@@ -135,7 +141,9 @@ int attn_prefill_strided(const void *q, const void *k, const void *v, void *o, f
  *            (ATTN_DEV_SEQLEN_CLAMPED)
  *   o        [B, Hq, Sq, D], bf16 or fp32 by out_dtype; lse [B, Hq, Sq] fp32 or NULL
  * Requires Hq % Hkv == 0, D in {64, 128}. Same tensor-core kernel as attn_prefill (with
- * seqlens[b] = Sq = S, max_len = S it computes exactly attn_prefill's result).
+ * seqlens[b] = Sq = S, max_len = S it computes exactly attn_prefill's result), including the
+ * fp16 copy of V in the library-owned scratch (B*Hkv*max_len*D*2 bytes; only the key tiles
+ * below each seqlens[b] are written) and the same fallback when the scratch is unavailable.
  * Sources: "Hand-written Triton decoder" (m.nlpx.cn/news/28229) section 1.4 (speculative
  * decoding and beam search reuse the attention kernels with several new tokens);
  * "Attention three-op fusion" (xdnf.cn/news/349386) section 4.3 (causal and padding masks).
