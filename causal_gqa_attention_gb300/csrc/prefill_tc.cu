@@ -5,8 +5,8 @@
 //
 // One thread block owns 256 consecutive query rows of one (batch, query head): two 128-row
 // Q tiles (HD = 128; half as wide at 64). Both tiles consume the same stream of 128-key K/V
-// tiles, so every K/V tile brought in by TMA feeds four tensor-core products. Roles (12 warps;
-// 10 when V comes pre-converted, see below):
+// tiles, so every K/V tile brought in by TMA feeds four tensor-core products. Roles (12 warps,
+// three warpgroups; the first gives registers to the other two at entry):
 //   warp 0      TMA producer: Q tiles once, then K_j into a 2-stage and V_j into a 3-stage ring
 //               (V also waits for its conversion, so it gets one stage more);
 //   warp 1      tcgen05 issuer (the warp runs converged, one elected lane issues each MMA):
@@ -14,7 +14,7 @@
 //               TMEM allocation;
 //   warps 2-3   convert each landed V tile from bf16 to fp16 in place (see below), unless
 //               V was converted beforehand;
-//   warps 4-7   softmax for tile 0, warps 8-11 for tile 1 (2-5 and 6-9 with pre-converted V):
+//   warps 4-7   softmax for tile 0, warps 8-11 for tile 1:
 //               one thread per query row (its TMEM lane). Reads the 128 scores of its row,
 //               masks, updates the running max and sum, writes P (fp16) over the scores it
 //               came from, rescales its O row when the max moved, and finally writes O / l
@@ -69,9 +69,14 @@ namespace {
 
 constexpr int BM = 128;        // query rows per tile = TMEM lanes
 constexpr int BN = 128;        // keys per K/V tile
-// 12 warps when the kernel converts V itself, 10 when V arrives converted (no converter warps)
-template <bool VPRE>
-constexpr int kThreads = VPRE ? 320 : 384;
+constexpr int kThreads = 384;  // 12 warps = 3 warpgroups
+// Registers per thread: the block is compiled for (and launched with) kRegsLaunch; at entry the
+// producer / issuer / converter warpgroup gives registers back (kRegsLow) and the two softmax
+// warpgroups, which hold a row of 128 scores per thread, take them (kRegsHigh). Each SMSP holds
+// one warp of each warpgroup. An increase that the block's pool cannot cover would wait
+// forever, so the host checks the compiled count before the first launch.
+constexpr int kRegsLaunch = 168, kRegsLow = 136, kRegsHigh = 184;
+static_assert(kRegsLow * 128 + kRegsHigh * 256 <= kRegsLaunch * kThreads, "register pool");
 constexpr uint32_t kBox = 16384;          // one 128-row x 64-col bf16 box (128-byte rows)
 constexpr int KST = 2;                    // K ring stages
 constexpr int VST = 3;                    // V ring stages (V also waits for its fp16 conversion)
@@ -177,10 +182,10 @@ __device__ __noinline__ void zero_v_tail(uint4 *tile, int ct, int rows_ok, int n
 // SPLIT = true: one block per (row block, key segment of J tiles, head, batch); it writes the
 // segment's normalised O (fp32) and its LSE (log2 units) to ws_o / ws_lse, and
 // prefill_split_merge_kernel combines the segments of each row.
-// VPRE = true: tv maps an fp16 copy of V written by convert_v_kernel (no converter warps; the
-// softmax warps are 2-9). VPRE = false: tv maps the bf16 V, converted on chip by warps 2-3.
+// VPRE = true: tv maps an fp16 copy of V written by convert_v_kernel (warps 2-3 have nothing to
+// do). VPRE = false: tv maps the bf16 V, converted on chip by warps 2-3.
 template <int HD, bool OUT_F32, bool SPLIT, bool VPRE>
-__global__ void __launch_bounds__(kThreads<VPRE>, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, void *__restrict__ out,
                       float *__restrict__ lse, int B, int S, int Hq, int Hkv, float scale_log2,
@@ -199,7 +204,7 @@ __global__ void __launch_bounds__(kThreads<VPRE>, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    constexpr int kSoftmaxWarp0 = VPRE ? 2 : 4;  // first of the 8 softmax warps
+    constexpr int kSoftmaxWarp0 = 4;  // first of the 8 softmax warps
 
     // ---- work item: heaviest row blocks first (causal), heads of one group adjacent
     const int n_rb = (S + 2 * BM - 1) / (2 * BM);
@@ -274,6 +279,8 @@ __global__ void __launch_bounds__(kThreads<VPRE>, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
     if (warp == 0) {
         // ================================================================ TMA producer
         if (lane == 0) {
@@ -413,7 +420,9 @@ __global__ void __launch_bounds__(kThreads<VPRE>, 1)
             mbar_arrive(&bar[B_VREADY + s]);
         }
         if (over) atomicOr(status, 4u);
-    } else if (warp >= kSoftmaxWarp0) {
+    }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
         // ================================================================ softmax / epilogue
         const int t = (warp - kSoftmaxWarp0) / 4;
         const int wq = warp & 3;
@@ -747,6 +756,11 @@ cudaError_t launch_t(const PrefillTcArgs &a, cudaStream_t st)
         e = cudaFuncSetAttribute(prefill_tc_kernel<HD, OUT_F32, SPLIT, VPRE>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<HD>::kSmem);
         if (e != cudaSuccess) return e;
+        // the warpgroups' register split assumes exactly kRegsLaunch registers per thread
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<HD, OUT_F32, SPLIT, VPRE>);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
         if (dev < 64) attr_set[dev] = true;
     }
     const int n_rb = (a.S + 2 * BM - 1) / (2 * BM);
@@ -763,7 +777,7 @@ cudaError_t launch_t(const PrefillTcArgs &a, cudaStream_t st)
     {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)blocks);
-        cfg.blockDim = dim3(kThreads<VPRE>);
+        cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = Geo<HD>::kSmem;
         cfg.stream = st;
         cfg.attrs = pdl;
