@@ -43,6 +43,7 @@ import workloads  # noqa: E402
 
 PREFILL = workloads.CONFIGS["c5b"]
 DECODE = workloads.CONFIGS["c4b"]
+E2E_CHUNKS = 4  # batch slices of the end-to-end prefill (upload / compute / download overlap)
 METRIC = "prefill attention TFLOP/s and decode KV-read GB/s, % of GB300 roofline"
 FLUSH_BYTES = 512 << 20
 # Nominal GB300 figures, reported beside the measured peaks: dense bf16 tensor throughput and
@@ -568,40 +569,50 @@ def main():
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdq, hdk, hdv, hdsl))
         d2h = ho.numel() * ho.element_size() + hdo.numel() * hdo.element_size()
 
-        copy_stream = torch.cuda.Stream(device=dev)
+        up_stream = torch.cuda.Stream(device=dev)
+        down_stream = torch.cuda.Stream(device=dev)
         oo = torch.empty_like(q)
         od = torch.empty_like(do)
+        nch = E2E_CHUNKS if PREFILL.B % E2E_CHUNKS == 0 else 1
+        cb = PREFILL.B // nch
 
         def e2e_step():
-            # the step's copies overlap its compute where the data allows: the decode inputs
-            # go up while the prefill runs, the prefill output comes down while decode runs
-            ev_in = torch.cuda.Event()
-            ev_pre = torch.cuda.Event()
+            # The host link (not the GPU) bounds this step, so the prefill runs as nch calls on
+            # batch slices: slice c's upload overlaps slice c-1's prefill and its output goes
+            # down while slice c+1 computes; the decode inputs go up behind the last slice.
+            ev_in = [torch.cuda.Event() for _ in range(nch)]
+            ev_pre = [torch.cuda.Event() for _ in range(nch)]
             ev_dec_in = torch.cuda.Event()
             ev_dec = torch.cuda.Event()
-            copy_stream.wait_stream(stream)  # the previous step is done with every buffer
-            with torch.cuda.stream(copy_stream):
-                dq2.copy_(hq, non_blocking=True)
-                dk2.copy_(hk, non_blocking=True)
-                dv2.copy_(hv, non_blocking=True)
-                ev_in.record(copy_stream)
+            up_stream.wait_stream(stream)  # the previous step is done with every buffer
+            down_stream.wait_stream(stream)
+            with torch.cuda.stream(up_stream):
+                for c in range(nch):
+                    sl = slice(c * cb, (c + 1) * cb)
+                    dq2[sl].copy_(hq[sl], non_blocking=True)
+                    dk2[sl].copy_(hk[sl], non_blocking=True)
+                    dv2[sl].copy_(hv[sl], non_blocking=True)
+                    ev_in[c].record(up_stream)
                 ddq.copy_(hdq, non_blocking=True)
                 ddk.copy_(hdk, non_blocking=True)
                 ddv.copy_(hdv, non_blocking=True)
                 ddsl.copy_(hdsl, non_blocking=True)
-                ev_dec_in.record(copy_stream)
-            stream.wait_event(ev_in)
-            cga.prefill(dq2, dk2, dv2, causal=True, out=oo)
-            ev_pre.record(stream)
+                ev_dec_in.record(up_stream)
+            for c in range(nch):
+                sl = slice(c * cb, (c + 1) * cb)
+                stream.wait_event(ev_in[c])
+                cga.prefill(dq2[sl], dk2[sl], dv2[sl], causal=True, out=oo[sl])
+                ev_pre[c].record(stream)
+                with torch.cuda.stream(down_stream):
+                    down_stream.wait_event(ev_pre[c])
+                    ho[sl].copy_(oo[sl], non_blocking=True)
             stream.wait_event(ev_dec_in)
             cga.decode(ddq, ddk, ddv, ddsl, out=od)
             ev_dec.record(stream)
-            with torch.cuda.stream(copy_stream):
-                copy_stream.wait_event(ev_pre)
-                ho.copy_(oo, non_blocking=True)
-                copy_stream.wait_event(ev_dec)
+            with torch.cuda.stream(down_stream):
+                down_stream.wait_event(ev_dec)
                 hdo.copy_(od, non_blocking=True)
-            stream.wait_stream(copy_stream)  # the step ends when its results are on the host
+            stream.wait_stream(down_stream)  # the step ends when its results are on the host
 
         for _ in range(2):
             e2e_step()
@@ -619,7 +630,8 @@ def main():
         e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, world, dev)
         e2e = {"value": pflops * world / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
-               "note": "prefill flops over the whole step incl. decode and host copies"}
+               "note": "prefill flops over the whole step incl. decode and host copies",
+               "prefill_calls_per_step": nch}
 
     extras = None
     if not args.no_extras and args.only == "all":
