@@ -22,7 +22,9 @@ from ._lib import (ATTN_BF16, ATTN_DEV_FP16_RANGE, ATTN_DEV_SEQLEN_CLAMPED, ATTN
                    ATTN_ERR_WORKSPACE, ATTN_F32, ATTN_OK, AttnError)
 
 __all__ = [
-    "attn_prefill", "attn_prefill_ex", "attn_prefill_strided", "attn_prefill_varlen", "prefill_varlen", "attn_chunk", "attn_decode", "attn_decode_ex",
+    "attn_prefill", "attn_prefill_ex", "attn_prefill_strided", "attn_prefill_varlen",
+    "attn_prefill_varlen_strided", "prefill_varlen", "attn_chunk", "attn_chunk_strided",
+    "attn_decode", "attn_decode_ex",
     "attn_decode_noalloc", "chunk", "attn_decode_rope", "decode_rope",
     "attn_decode_workspace_bytes", "attn_decode_chunk_len", "attn_reserve_workspace",
     "attn_device_status", "attn_status_string", "attn_version", "prefill", "decode",
@@ -66,6 +68,21 @@ def attn_chunk(q, kcache, vcache, seqlens, o, lse, B, Sq, Hq, Hkv, D, max_len, s
                out_dtype, stream):
     return _lib.load().attn_chunk(q, kcache, vcache, seqlens, o, lse, B, Sq, Hq, Hkv, D, max_len,
                                   scale, causal, out_dtype, stream)
+
+
+def attn_chunk_strided(q, kcache, vcache, seqlens, o, lse, B, Sq, Hq, Hkv, D, max_len, q_strides,
+                       k_strides, v_strides, o_strides, scale, causal, out_dtype, stream):
+    return _lib.load().attn_chunk_strided(q, kcache, vcache, seqlens, o, lse, B, Sq, Hq, Hkv, D,
+                                          max_len, q_strides, k_strides, v_strides, o_strides,
+                                          scale, causal, out_dtype, stream)
+
+
+def attn_prefill_varlen_strided(q, k, v, seqlens, o, lse, B, S, Hq, Hkv, D, q_strides,
+                                k_strides, v_strides, o_strides, scale, causal, out_dtype,
+                                stream):
+    return _lib.load().attn_prefill_varlen_strided(q, k, v, seqlens, o, lse, B, S, Hq, Hkv, D,
+                                                   q_strides, k_strides, v_strides, o_strides,
+                                                   scale, causal, out_dtype, stream)
 
 
 def attn_decode(q, kcache, vcache, seqlens, o, B, Hq, Hkv, D, max_len, scale, stream):
@@ -224,28 +241,43 @@ def chunk(q, kcache, vcache, seqlens, causal: bool = True, scale: float | None =
     """Sq new queries per sequence against a bf16 KV cache: q [B,Hq,Sq,D] bf16 (the last Sq
     tokens of each sequence, already in the cache), caches [B,Hkv,max_len,D] bf16, seqlens [B]
     int32 on the device. Query i of sequence b sits at position seqlens[b] - Sq + i.
-    Returns o [B,Hq,Sq,D] (bf16 by default), or (o, lse [B,Hq,Sq])."""
+    Returns o [B,Hq,Sq,D] (bf16 by default), or (o, lse [B,Hq,Sq]).
+
+    q, the caches and ``out`` may be views with any strides whose head dim is contiguous, e.g.
+    caches stored [B,max_len,Hkv,D] and passed as ``cache.transpose(1, 2)``."""
     torch = _torch()
     B, Hq, Sq, D = q.shape
     Hkv, max_len = kcache.shape[1], kcache.shape[2]
     if kcache.shape != (B, Hkv, max_len, D) or vcache.shape != kcache.shape:
         raise ValueError("cache shapes do not match q")
-    _check_cuda("q", q, torch.bfloat16)
-    _check_cuda("kcache", kcache, torch.bfloat16)
-    _check_cuda("vcache", vcache, torch.bfloat16)
     _check_cuda("seqlens", seqlens, torch.int32)
     if seqlens.shape != (B,):
         raise ValueError("seqlens must be [B]")
     out_dtype = out_dtype or torch.bfloat16
     if out is None:
         out = torch.empty((B, Hq, Sq, D), dtype=out_dtype, device=q.device)
-    else:
-        _check_cuda("out", out, out_dtype)
+    elif out.shape != (B, Hq, Sq, D):
+        raise ValueError(f"out must be [B,Hq,Sq,D], got {tuple(out.shape)}")
     if return_lse and lse is None:
         lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     out_t = ATTN_BF16 if out_dtype == torch.bfloat16 else ATTN_F32
+    views = (("q", q, torch.bfloat16), ("kcache", kcache, torch.bfloat16),
+             ("vcache", vcache, torch.bfloat16), ("out", out, out_dtype))
+    if not all(t.is_contiguous() for _, t, _ in views):
+        for n, t, dt in views:
+            _check_view(n, t, dt)
+        with torch.cuda.device(q.device):
+            rc = attn_chunk_strided(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(seqlens),
+                                    _ptr(out), _ptr(lse), B, Sq, Hq, Hkv, D, max_len,
+                                    _bshd_strides(q), _bshd_strides(kcache),
+                                    _bshd_strides(vcache), _bshd_strides(out), float(scale),
+                                    int(bool(causal)), out_t, _stream_handle(q.device))
+        _lib.check("attn_chunk_strided", rc)
+        return (out, lse) if return_lse else out
+    for n, t, dt in views:
+        _check_cuda(n, t, dt)
     with torch.cuda.device(q.device):
         rc = attn_chunk(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(seqlens), _ptr(out), _ptr(lse),
                         B, Sq, Hq, Hkv, D, max_len, float(scale), int(bool(causal)), out_t,
@@ -257,27 +289,43 @@ def chunk(q, kcache, vcache, seqlens, causal: bool = True, scale: float | None =
 def prefill_varlen(q, k, v, seqlens, causal: bool = True, scale: float | None = None,
                    out_dtype=None, return_lse: bool = False, out=None, lse=None):
     """Padded batch: q [B,Hq,S,D], k/v [B,Hkv,S,D] bf16, sequence b valid in its first seqlens[b]
-    tokens (seqlens int32 on the device). Padding rows give o = 0 (lse = -inf)."""
+    tokens (seqlens int32 on the device). Padding rows give o = 0 (lse = -inf).
+
+    q, k, v and ``out`` may be views with any strides whose head dim is contiguous (e.g. head
+    slices of a padded fused QKV projection output)."""
     torch = _torch()
     B, Hq, S, D = q.shape
     Hkv = k.shape[1]
     if k.shape != (B, Hkv, S, D) or v.shape != k.shape:
         raise ValueError("k/v shapes do not match q")
-    for n, t in (("q", q), ("k", k), ("v", v)):
-        _check_cuda(n, t, torch.bfloat16)
     _check_cuda("seqlens", seqlens, torch.int32)
     if seqlens.shape != (B,):
         raise ValueError("seqlens must be [B]")
     out_dtype = out_dtype or torch.bfloat16
     if out is None:
         out = torch.empty((B, Hq, S, D), dtype=out_dtype, device=q.device)
-    else:
-        _check_cuda("out", out, out_dtype)
+    elif out.shape != (B, Hq, S, D):
+        raise ValueError(f"out must be [B,Hq,S,D], got {tuple(out.shape)}")
     if return_lse and lse is None:
         lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     out_t = ATTN_BF16 if out_dtype == torch.bfloat16 else ATTN_F32
+    views = (("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
+             ("out", out, out_dtype))
+    if not all(t.is_contiguous() for _, t, _ in views):
+        for n, t, dt in views:
+            _check_view(n, t, dt)
+        with torch.cuda.device(q.device):
+            rc = attn_prefill_varlen_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(seqlens), _ptr(out),
+                                             _ptr(lse), B, S, Hq, Hkv, D, _bshd_strides(q),
+                                             _bshd_strides(k), _bshd_strides(v),
+                                             _bshd_strides(out), float(scale),
+                                             int(bool(causal)), out_t, _stream_handle(q.device))
+        _lib.check("attn_prefill_varlen_strided", rc)
+        return (out, lse) if return_lse else out
+    for n, t, dt in views:
+        _check_cuda(n, t, dt)
     with torch.cuda.device(q.device):
         rc = attn_prefill_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(seqlens), _ptr(out), _ptr(lse), B,
                                  S, Hq, Hkv, D, float(scale), int(bool(causal)), out_t,

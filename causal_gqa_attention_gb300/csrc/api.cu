@@ -339,7 +339,25 @@ int attn_prefill_strided(const void *q, const void *k, const void *v, void *o, f
 namespace {
 int chunk_or_varlen(const void *q, const void *kc, const void *vc, const int *seqlens, void *o,
                     float *lse, int B, int Sq, int Hq, int Hkv, int D, int max_len, float scale,
-                    int causal, int out_dtype, int front, void *stream);
+                    int causal, int out_dtype, int front, const Strides &qs, const Strides &ks,
+                    const Strides &vs, const Strides &os, void *stream);
+
+// Strides from three host int64 arrays {batch, token, head}: ATTN_ERR_INVALID for a NULL array,
+// ATTN_ERR_ALIGN for strides the tensor maps or the output stores cannot use.
+int read_strides(const long long *qa, const long long *ka, const long long *va,
+                 const long long *oa, int out_dtype, Strides *qs, Strides *ks, Strides *vs,
+                 Strides *os)
+{
+    if (!qa || !ka || !va || !oa) return ATTN_ERR_INVALID;
+    *qs = Strides{qa[0], qa[1], qa[2]};
+    *ks = Strides{ka[0], ka[1], ka[2]};
+    *vs = Strides{va[0], va[1], va[2]};
+    *os = Strides{oa[0], oa[1], oa[2]};
+    if (!strides_ok(*qs, 2) || !strides_ok(*ks, 2) || !strides_ok(*vs, 2) ||
+        !strides_ok(*os, out_dtype == ATTN_F32 ? 4 : 2))
+        return ATTN_ERR_ALIGN;
+    return ATTN_OK;
+}
 }  // namespace
 
 int attn_prefill_varlen(const void *q, const void *k, const void *v, const int *seqlens, void *o,
@@ -347,7 +365,22 @@ int attn_prefill_varlen(const void *q, const void *k, const void *v, const int *
                         int out_dtype, void *stream)
 {
     return chunk_or_varlen(q, k, v, seqlens, o, lse, B, S, Hq, Hkv, D, S, scale, causal,
-                           out_dtype, 1, stream);
+                           out_dtype, 1, contiguous(Hq, S, D), contiguous(Hkv, S, D),
+                           contiguous(Hkv, S, D), contiguous(Hq, S, D), stream);
+}
+
+int attn_prefill_varlen_strided(const void *q, const void *k, const void *v, const int *seqlens,
+                                void *o, float *lse, int B, int S, int Hq, int Hkv, int D,
+                                const long long *q_strides, const long long *k_strides,
+                                const long long *v_strides, const long long *o_strides,
+                                float scale, int causal, int out_dtype, void *stream)
+{
+    Strides qs, ks, vs, os;
+    int rc = read_strides(q_strides, k_strides, v_strides, o_strides, out_dtype, &qs, &ks, &vs,
+                          &os);
+    if (rc != ATTN_OK) return rc;
+    return chunk_or_varlen(q, k, v, seqlens, o, lse, B, S, Hq, Hkv, D, S, scale, causal,
+                           out_dtype, 1, qs, ks, vs, os, stream);
 }
 
 int attn_chunk(const void *q, const void *kcache, const void *vcache, const int *seqlens,
@@ -355,7 +388,23 @@ int attn_chunk(const void *q, const void *kcache, const void *vcache, const int 
                float scale, int causal, int out_dtype, void *stream)
 {
     return chunk_or_varlen(q, kcache, vcache, seqlens, o, lse, B, Sq, Hq, Hkv, D, max_len, scale,
-                           causal, out_dtype, 0, stream);
+                           causal, out_dtype, 0, contiguous(Hq, Sq, D),
+                           contiguous(Hkv, max_len, D), contiguous(Hkv, max_len, D),
+                           contiguous(Hq, Sq, D), stream);
+}
+
+int attn_chunk_strided(const void *q, const void *kcache, const void *vcache, const int *seqlens,
+                       void *o, float *lse, int B, int Sq, int Hq, int Hkv, int D, int max_len,
+                       const long long *q_strides, const long long *k_strides,
+                       const long long *v_strides, const long long *o_strides, float scale,
+                       int causal, int out_dtype, void *stream)
+{
+    Strides qs, ks, vs, os;
+    int rc = read_strides(q_strides, k_strides, v_strides, o_strides, out_dtype, &qs, &ks, &vs,
+                          &os);
+    if (rc != ATTN_OK) return rc;
+    return chunk_or_varlen(q, kcache, vcache, seqlens, o, lse, B, Sq, Hq, Hkv, D, max_len, scale,
+                           causal, out_dtype, 0, qs, ks, vs, os, stream);
 }
 
 }  // extern "C"
@@ -363,7 +412,8 @@ int attn_chunk(const void *q, const void *kcache, const void *vcache, const int 
 namespace {
 int chunk_or_varlen(const void *q, const void *kcache, const void *vcache, const int *seqlens,
                     void *o, float *lse, int B, int Sq, int Hq, int Hkv, int D, int max_len,
-                    float scale, int causal, int out_dtype, int front, void *stream)
+                    float scale, int causal, int out_dtype, int front, const Strides &qs,
+                    const Strides &ks, const Strides &vs, const Strides &os, void *stream)
 {
     if (!seqlens) return ATTN_ERR_INVALID;
     if (max_len <= 0) return ATTN_ERR_INVALID;
@@ -374,11 +424,10 @@ int chunk_or_varlen(const void *q, const void *kcache, const void *vcache, const
     if ((long long)B * Hkv * max_len > (1LL << 40)) return ATTN_ERR_UNSUPPORTED;
     PrefillTcArgs a;
     std::memset(&a, 0, sizeof(a));
-    if (!encode_bf16_4d(&a.tq, q, D, Sq, Hq, B, contiguous(Hq, Sq, D)) ||
-        !encode_bf16_4d(&a.tk, kcache, D, max_len, Hkv, B, contiguous(Hkv, max_len, D)) ||
-        !encode_bf16_4d(&a.tv, vcache, D, max_len, Hkv, B, contiguous(Hkv, max_len, D)))
+    if (!encode_bf16_4d(&a.tq, q, D, Sq, Hq, B, qs) ||
+        !encode_bf16_4d(&a.tk, kcache, D, max_len, Hkv, B, ks) ||
+        !encode_bf16_4d(&a.tv, vcache, D, max_len, Hkv, B, vs))
         return ATTN_ERR_CUDA;
-    const Strides os = contiguous(Hq, Sq, D);
     a.o = o;
     a.o_sb = os.b;
     a.o_ss = os.s;
@@ -404,13 +453,13 @@ int chunk_or_varlen(const void *q, const void *kcache, const void *vcache, const
     rc = prefill_scratch(a, 0, 0, (size_t)B * Hkv * max_len * D * 2, st);
     if (rc != ATTN_OK) return rc;
     if (a.vpre) {
-        const Strides cs = contiguous(Hkv, max_len, D);
         a.v_src = vcache;
-        a.v_sb = cs.b;
-        a.v_ss = cs.s;
-        a.v_sh = cs.h;
+        a.v_sb = vs.b;
+        a.v_ss = vs.s;
+        a.v_sh = vs.h;
         a.v_rows = max_len;
-        if (!encode_bf16_4d(&a.tv, a.v16, D, max_len, Hkv, B, cs, true)) return ATTN_ERR_CUDA;
+        if (!encode_bf16_4d(&a.tv, a.v16, D, max_len, Hkv, B, contiguous(Hkv, max_len, D), true))
+            return ATTN_ERR_CUDA;
     }
     return cuda_status(gqa::launch_prefill_tc(a, out_dtype == ATTN_F32,
                                               static_cast<cudaStream_t>(stream)));

@@ -153,6 +153,21 @@ int attn_chunk(const void *q, const void *kcache, const void *vcache, const int 
                float scale, int causal, int out_dtype, void *stream);
 
 /*
+ * attn_chunk_strided -- attn_chunk for operands in any layout whose head dim is contiguous,
+ * described as for attn_prefill_strided by three int64 element strides {batch, token, head}
+ * per operand: q and o over Sq tokens, the caches over max_len rows. Element (b, g, r, d) of
+ * kcache is kcache[b*k_strides[0] + r*k_strides[1] + g*k_strides[2] + d]; e.g. caches stored
+ * [B, max_len, Hkv, D] have strides {max_len*Hkv*D, Hkv*D, D}. NULL stride arrays return
+ * ATTN_ERR_INVALID; strides that are not positive multiples of 16 bytes, ATTN_ERR_ALIGN. The
+ * fp16 copy of V it makes (as attn_chunk) is contiguous. Other arguments as attn_chunk.
+ */
+int attn_chunk_strided(const void *q, const void *kcache, const void *vcache, const int *seqlens,
+                       void *o, float *lse, int B, int Sq, int Hq, int Hkv, int D, int max_len,
+                       const long long *q_strides, const long long *k_strides,
+                       const long long *v_strides, const long long *o_strides, float scale,
+                       int causal, int out_dtype, void *stream);
+
+/*
  * attn_prefill_varlen -- batched prefill of sequences of different lengths, padded to S tokens.
  * Sequence b holds seqlens[b] valid tokens at positions 0 .. seqlens[b]-1 of q, k, v; keys at
  * or past seqlens[b] are masked (their contents never reach the result); padding rows
@@ -166,6 +181,20 @@ int attn_chunk(const void *q, const void *kcache, const void *vcache, const int 
 int attn_prefill_varlen(const void *q, const void *k, const void *v, const int *seqlens, void *o,
                         float *lse, int B, int S, int Hq, int Hkv, int D, float scale, int causal,
                         int out_dtype, void *stream);
+
+/*
+ * attn_prefill_varlen_strided -- attn_prefill_varlen for operands in any layout whose head dim
+ * is contiguous ({batch, token, head} element strides per operand, as attn_prefill_strided;
+ * e.g. q, k, v as head slices of a padded fused QKV projection output [B, S, Hq+2*Hkv, D], o
+ * written into a [B, S, Hq, D] buffer). NULL stride arrays return ATTN_ERR_INVALID; strides
+ * that are not positive multiples of 16 bytes, ATTN_ERR_ALIGN. Other arguments as
+ * attn_prefill_varlen.
+ */
+int attn_prefill_varlen_strided(const void *q, const void *k, const void *v, const int *seqlens,
+                                void *o, float *lse, int B, int S, int Hq, int Hkv, int D,
+                                const long long *q_strides, const long long *k_strides,
+                                const long long *v_strides, const long long *o_strides,
+                                float scale, int causal, int out_dtype, void *stream);
 
 /*
  * attn_decode -- one query token per sequence against a bf16 KV cache.

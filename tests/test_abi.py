@@ -95,6 +95,23 @@ def test_prefill_strided_rejects_on_host(lib, strides, code):
                                     None) == code
 
 
+@pytest.mark.parametrize("strides,code", [
+    ((None, (8, 8, 8), (8, 8, 8), (8, 8, 8)), 1),                     # NULL stride array
+    (((1024, 132, 8), (8, 8, 8), (8, 8, 8), (8, 8, 8)), 3),           # q token stride 264 B
+    (((1024, 128, 8), (8, 8, 4), (8, 8, 8), (8, 8, 8)), 3),           # cache head stride 8 B
+    (((1024, 128, 8), (8, 8, 8), (0, 8, 8), (8, 8, 8)), 3),           # cache batch stride 0
+    (((1024, 128, 8), (8, 8, 8), (8, 8, 8), (8, 8, -8)), 3),          # negative o stride
+])
+def test_chunk_and_varlen_strided_reject_on_host(lib, strides, code):
+    arrs = [None if st is None else _ll3(*st) for st in strides]
+    # q, kc, vc, seqlens, o, lse, B, Sq, Hq, Hkv, D, max_len, strides x4, scale, causal, out
+    assert lib.attn_chunk_strided(A16, A16, A16, A16, A16, None, 1, 8, 2, 1, 64, 64, *arrs, 0.1,
+                                  1, 1, None) == code
+    # q, k, v, seqlens, o, lse, B, S, Hq, Hkv, D, strides x4, scale, causal, out
+    assert lib.attn_prefill_varlen_strided(A16, A16, A16, A16, A16, None, 1, 8, 2, 1, 64, *arrs,
+                                           0.1, 1, 1, None) == code
+
+
 def test_prefill_strided_fp32_out_stride(lib):
     # an o token stride of 6 fp32 elements (24 B) is not a 16-byte multiple
     ok = _ll3(1024, 128, 8)

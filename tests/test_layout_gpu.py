@@ -143,3 +143,57 @@ def test_strided_equals_contiguous_bitwise():
     o1, l1 = _run(qd, kd, vd, True, torch.bfloat16)
     o2, l2 = _run(_bshd(q, dev), _bshd(k, dev), _bshd(v, dev), True, torch.bfloat16)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_chunk_strided_caches_bitwise_equal_contiguous():
+    """A chunk against caches stored [B, max_len, Hkv, D] (passed as transposed views), q as a
+    [B, Sq, Hq, D] view and O written into a [B, Sq, Hq, D] buffer: the oracle's result, and the
+    same bits as the contiguous call."""
+    cga = library()
+    dev = device()
+    B, Hq, Hkv, Sq, max_len = 3, 8, 2, 200, 700
+    q, kc, vc, sl = workloads.decode_inputs(B, Hq, Hkv, 128, max_len, "explicit", seed=13,
+                                            seqlens=[700, 200, 450])
+    qc = workloads.prefill_inputs(B, Hq, Hkv, Sq, 128, "bf16", seed=14)[0]
+    o_ref, lse_ref = oracle.chunk(qc, kc, vc, sl, 1 / math.sqrt(128), True)
+    kv_, vv_, qv_ = _bshd(kc, dev), _bshd(vc, dev), _bshd(qc, dev)
+    assert not kv_.is_contiguous()
+    o_store = torch.full((B, Sq, Hq, 128), float("nan"), dtype=torch.float32, device=dev)
+    o, lse = cga.chunk(qv_, kv_, vv_, sl.to(dev), out=o_store.transpose(1, 2),
+                       out_dtype=torch.float32, return_lse=True)
+    torch.cuda.synchronize()
+    assert cga.device_status() == 0
+    check_out(o_store.transpose(1, 2), o_ref, "bf16_pre", "strided chunk")
+    check_lse(lse, lse_ref, "strided chunk lse")
+    o2, l2 = cga.chunk(qc.to(dev), kc.to(dev), vc.to(dev), sl.to(dev), out_dtype=torch.float32,
+                       return_lse=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o_store.transpose(1, 2), o2) and torch.equal(lse, l2)
+
+
+@pytest.mark.parametrize("D", [128, 64])
+def test_varlen_from_fused_qkv(D):
+    """A padded batch read as head slices of one [B, S, Hq + 2 Hkv, D] projection output (K and V
+    NaN past each length), O written into a [B, S, Hq, D] buffer, against the oracle."""
+    dev = device()
+    B, Hq, Hkv, S = 3, 8, 2, 600
+    q, k, v = workloads.prefill_inputs(B, Hq, Hkv, S, D, "bf16", seed=15)
+    lens = [600, 1, 333]
+    for b, L in enumerate(lens):
+        k[b, :, L:] = float("nan")
+        v[b, :, L:] = float("nan")
+    sl = torch.tensor(lens, dtype=torch.int32)
+    o_ref, lse_ref = oracle.prefill_varlen(q, k, v, sl, True, 1 / math.sqrt(D))
+    qkv = torch.cat([q.transpose(1, 2), k.transpose(1, 2), v.transpose(1, 2)], dim=2)
+    qkv = qkv.contiguous().to(dev)
+    qv = qkv[:, :, :Hq].transpose(1, 2)
+    kv = qkv[:, :, Hq:Hq + Hkv].transpose(1, 2)
+    vv = qkv[:, :, Hq + Hkv:].transpose(1, 2)
+    o_store = torch.full((B, S, Hq, D), float("nan"), dtype=torch.float32, device=dev)
+    cga = library()
+    _, lse = cga.prefill_varlen(qv, kv, vv, sl.to(dev), out=o_store.transpose(1, 2),
+                                out_dtype=torch.float32, return_lse=True)
+    torch.cuda.synchronize()
+    assert cga.device_status() == 0
+    check_out(o_store.transpose(1, 2), o_ref, "bf16_pre", f"fused-qkv varlen D{D}")
+    check_lse(lse, lse_ref, f"fused-qkv varlen D{D} lse")
