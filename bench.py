@@ -63,8 +63,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-extras", action="store_true",
-                   help="skip the extra timings (cache chunk, padded varlen, fused-QKV and "
-                        "head-dim-64 prefill, decode with RoPE)")
+                   help="skip the extra timings (the other configured workloads; cache chunk, "
+                        "padded varlen, fused-QKV and head-dim-64 prefill, decode with RoPE)")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle sample")
     p.add_argument("--only", default="all", choices=["all", "prefill", "decode"],
@@ -438,6 +438,74 @@ def time_extras(cga, dev, stream, flush, steps):
     return out
 
 
+def time_configs(cga, dev, stream, flush, pk, steps):
+    """Every configured workload besides the headline pair, timed with the same L2 flush and CUDA
+    events (median of the reps; one call each unless stated). Prefill: TFLOP/s and the fraction
+    of the measured bf16 peak (the fp32 parity workloads run on CUDA cores, no roofline claim).
+    Decode B1 L4096: one call, and back to back in a CUDA graph over enough caches (40 x 4.2 MB)
+    that consecutive calls never find their cache in L2."""
+    out = {}
+    reps = max(10, steps)
+    for name in ("c1", "c2", "c3", "c5a"):
+        cfg = workloads.CONFIGS[name]
+        q, k, v = [t.to(dev) for t in workloads.config_prefill_inputs(cfg)]
+        o = torch.empty(q.shape, dtype=q.dtype, device=dev)
+        for causal in cfg.causal:
+            ms = _time(lambda: cga.prefill(q, k, v, causal=causal, out=o), flush, stream, reps)
+            fl = workloads.prefill_flops(cfg.B, cfg.Hq, cfg.S, cfg.D, causal)
+            tf = fl / (ms * 1e-3) / 1e12
+            key = f"{name}_{'causal' if causal else 'noncausal'}"
+            row = {"workload": cfg.name, "ms": ms, "us": ms * 1e3, "value": tf,
+                   "unit": "TFLOP/s", "flops": fl, "dtype": cfg.dtype}
+            if cfg.dtype == "bf16":
+                row["frac_of_bf16_peak"] = tf / pk["bf16_tflops"]
+            else:
+                row["note"] = "fp32 I/O parity workload on CUDA cores (fp32 FMA): no roofline claim"
+            out[key] = row
+        del q, k, v, o
+    cfg = workloads.CONFIGS["c4a"]
+    q, kc, vc, sl = [t.to(dev) for t in workloads.config_decode_inputs(cfg, nan_fill=False)]
+    o = torch.empty_like(q)
+    by = workloads.decode_bytes(sl.cpu().tolist(), cfg.Hq, cfg.Hkv, cfg.D)
+    ms = _time(lambda: cga.decode(q, kc, vc, sl, out=o), flush, stream, max(20, reps))
+    row = {"workload": cfg.name, "us": ms * 1e3, "value": by / (ms * 1e-3) / 1e9, "unit": "GB/s",
+           "bytes": by, "frac": by / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]}
+    nsets = 40
+    sets = [[t.to(dev) for t in workloads.config_decode_inputs(cfg, seed=200 + i, nan_fill=False)]
+            for i in range(nsets)]
+    outs = [torch.empty_like(x[0]) for x in sets]
+    for (tq, tkc, tvc, tsl), to in zip(sets, outs):
+        cga.decode(tq, tkc, tvc, tsl, out=to)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for (tq, tkc, tvc, tsl), to in zip(sets, outs):
+            cga.decode(tq, tkc, tvc, tsl, out=to)
+    graph.replay()
+    torch.cuda.synchronize()
+    g_ms = statistics.median(_time_graph(graph, flush, stream, max(5, steps // 2)))
+    row["back_to_back"] = {"us_per_call": g_ms * 1e3 / nsets, "calls": nsets,
+                           "value": by * nsets / (g_ms * 1e-3) / 1e9, "unit": "GB/s",
+                           "frac": by * nsets / (g_ms * 1e-3) / 1e9 / pk["hbm_gbs"]}
+    out["c4a"] = row
+    del graph, sets, outs
+    return out
+
+
+def _time_graph(graph, flush, stream, reps):
+    ts = []
+    for _ in range(reps):
+        flush()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return ts
+
+
 # --------------------------------------------------------------------------- our kernels
 
 
@@ -634,8 +702,10 @@ def main():
                "prefill_calls_per_step": nch}
 
     extras = None
+    configs = None
     if not args.no_extras and args.only == "all":
         extras = time_extras(cga, dev, stream, flush_l2, args.steps)
+        configs = time_configs(cga, dev, stream, flush_l2, pk, args.steps)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -686,10 +756,11 @@ def main():
                          if args.prefill_batch is None and args.prefill_seq is None else None,
                          "kernel": "prefill_tc_kernel", "peak_source": pk["source"]},
             "e2e": e2e,
+            "configs": configs,
             "extras": extras,
             "cpu_baseline": cpu,
             "clocks": clocks,
-            "gpu_launches": 4 * args.steps,  # V conversion + prefill, decode stream + merge
+            "gpu_launches": 5 * args.steps,  # V conversion, V scale, prefill; decode stream + merge
             "wall_s_timed_region": t_wall,
         }
         print(json.dumps(line), flush=True)

@@ -17,20 +17,21 @@ from __future__ import annotations
 import math
 
 from . import _lib
-from ._lib import (ATTN_BF16, ATTN_DEV_FP16_RANGE, ATTN_DEV_SEQLEN_CLAMPED, ATTN_DEV_WAIT_TIMEOUT, ATTN_ERR_ALIGN,
+from ._lib import (ATTN_BF16, ATTN_DEV_SEQLEN_CLAMPED, ATTN_DEV_WAIT_TIMEOUT, ATTN_ERR_ALIGN,
                    ATTN_ERR_CUDA, ATTN_ERR_INVALID, ATTN_ERR_TIMEOUT, ATTN_ERR_UNSUPPORTED,
                    ATTN_ERR_WORKSPACE, ATTN_F32, ATTN_OK, AttnError)
 
 __all__ = [
-    "attn_prefill", "attn_prefill_ex", "attn_prefill_strided", "attn_prefill_varlen",
+    "attn_prefill", "attn_prefill_ex", "attn_prefill_ws", "attn_prefill_workspace_bytes",
+    "attn_reserve_workspace_bytes", "attn_prefill_strided", "attn_prefill_varlen",
     "attn_prefill_varlen_strided", "prefill_varlen", "attn_chunk", "attn_chunk_strided",
     "attn_decode", "attn_decode_ex",
     "attn_decode_noalloc", "chunk", "attn_decode_rope", "decode_rope",
     "attn_decode_workspace_bytes", "attn_decode_chunk_len", "attn_reserve_workspace",
-    "attn_device_status", "attn_status_string", "attn_version", "prefill", "decode",
+    "attn_device_status", "attn_debug_set_wait_limit", "attn_status_string", "attn_version", "prefill", "decode",
     "device_status", "AttnError", "ATTN_OK", "ATTN_ERR_INVALID", "ATTN_ERR_UNSUPPORTED",
     "ATTN_ERR_ALIGN", "ATTN_ERR_WORKSPACE", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "ATTN_F32",
-    "ATTN_BF16", "ATTN_DEV_FP16_RANGE", "ATTN_DEV_SEQLEN_CLAMPED", "ATTN_DEV_WAIT_TIMEOUT", "load_library",
+    "ATTN_BF16", "ATTN_DEV_SEQLEN_CLAMPED", "ATTN_DEV_WAIT_TIMEOUT", "load_library",
 ]
 
 
@@ -49,6 +50,20 @@ def attn_prefill_ex(q, k, v, o, lse, B, S, Hq, Hkv, D, scale, causal, in_dtype, 
                     stream):
     return _lib.load().attn_prefill_ex(q, k, v, o, lse, B, S, Hq, Hkv, D, scale, causal,
                                        in_dtype, out_dtype, stream)
+
+
+def attn_prefill_ws(q, k, v, o, lse, B, S, Hq, Hkv, D, scale, causal, out_dtype, workspace,
+                    workspace_bytes, stream):
+    return _lib.load().attn_prefill_ws(q, k, v, o, lse, B, S, Hq, Hkv, D, scale, causal,
+                                       out_dtype, workspace, workspace_bytes, stream)
+
+
+def attn_prefill_workspace_bytes(B, S, Hq, Hkv, D, causal):
+    return _lib.load().attn_prefill_workspace_bytes(B, S, Hq, Hkv, D, causal)
+
+
+def attn_reserve_workspace_bytes(nbytes):
+    return _lib.load().attn_reserve_workspace_bytes(nbytes)
 
 
 def attn_prefill_strided(q, k, v, o, lse, B, S, Hq, Hkv, D, q_strides, k_strides, v_strides,
@@ -122,6 +137,10 @@ def attn_reserve_workspace(B, Hq, Hkv, D, max_len):
     return _lib.load().attn_reserve_workspace(B, Hq, Hkv, D, max_len)
 
 
+def attn_debug_set_wait_limit(cycles):
+    return _lib.load().attn_debug_set_wait_limit(cycles)
+
+
 def attn_device_status(stream, status_ptr):
     return _lib.load().attn_device_status(stream, status_ptr)
 
@@ -186,7 +205,7 @@ def _check_view(name, t, dtype):
 
 
 def prefill(q, k, v, causal: bool = True, scale: float | None = None, out_dtype=None,
-            return_lse: bool = False, out=None, lse=None):
+            return_lse: bool = False, out=None, lse=None, workspace=None):
     """Attention forward with q_len = kv_len.
 
     q [B,Hq,S,D], k/v [B,Hkv,S,D], all bf16 (tensor-core path, D in {64,128}) or all fp32 (fp32
@@ -196,7 +215,11 @@ def prefill(q, k, v, causal: bool = True, scale: float | None = None, out_dtype=
 
     bf16 q, k, v (and ``out``) may be views with any strides as long as the head dim is
     contiguous, e.g. ``x.transpose(1, 2)`` of a [B,S,H,D] tensor, or head slices of a fused QKV
-    projection output viewed as [B,S,Hq+2Hkv,D]: they are read and written in place."""
+    projection output viewed as [B,S,Hq+2Hkv,D]: they are read and written in place.
+
+    ``workspace``: optional uint8 CUDA tensor (contiguous bf16 operands only) used as the call's
+    scratch instead of the library-owned buffer, so prefills on different streams can overlap;
+    ``attn_prefill_workspace_bytes`` gives the size that holds everything."""
     torch = _torch()
     B, Hq, S, D = q.shape
     Hkv = k.shape[1]
@@ -216,6 +239,8 @@ def prefill(q, k, v, causal: bool = True, scale: float | None = None, out_dtype=
     out_t = ATTN_BF16 if out_dtype == torch.bfloat16 else ATTN_F32
     views = (("q", q, q.dtype), ("k", k, q.dtype), ("v", v, q.dtype), ("out", out, out_dtype))
     if q.dtype == torch.bfloat16 and not all(t.is_contiguous() for _, t, _ in views):
+        if workspace is not None:
+            raise ValueError("a workspace needs contiguous q, k, v and out")
         for n, t, dt in views:
             _check_view(n, t, dt)
         with torch.cuda.device(q.device):
@@ -227,6 +252,17 @@ def prefill(q, k, v, causal: bool = True, scale: float | None = None, out_dtype=
         return (out, lse) if return_lse else out
     for n, t, dt in views:
         _check_cuda(n, t, dt)
+    if workspace is not None:
+        if q.dtype != torch.bfloat16:
+            raise ValueError("a workspace applies to bf16 inputs only")
+        _check_cuda("workspace", workspace)
+        with torch.cuda.device(q.device):
+            rc = attn_prefill_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, S, Hq, Hkv,
+                                 D, float(scale), int(bool(causal)), out_t, workspace.data_ptr(),
+                                 workspace.numel() * workspace.element_size(),
+                                 _stream_handle(q.device))
+        _lib.check("attn_prefill_ws", rc)
+        return (out, lse) if return_lse else out
     in_t = ATTN_BF16 if q.dtype == torch.bfloat16 else ATTN_F32
     with torch.cuda.device(q.device):
         rc = attn_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, S, Hq, Hkv, D,

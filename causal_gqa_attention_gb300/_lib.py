@@ -22,7 +22,6 @@ ATTN_F32 = 0
 ATTN_BF16 = 1
 ATTN_DEV_SEQLEN_CLAMPED = 0x1
 ATTN_DEV_WAIT_TIMEOUT = 0x2
-ATTN_DEV_FP16_RANGE = 0x4
 ATTN_DECODE_NOALLOC_SCRATCH_BYTES = 4 * 1024 * 1024
 
 _vp = ctypes.c_void_p
@@ -34,6 +33,9 @@ _sz = ctypes.c_size_t
 SIGNATURES = {
     "attn_prefill": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp]),
     "attn_prefill_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _i, _vp]),
+    "attn_prefill_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "attn_prefill_ws": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _vp, _sz,
+                             _vp]),
     "attn_prefill_strided": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp,
                                   _f, _i, _i, _vp]),
     "attn_prefill_varlen": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i,
@@ -52,6 +54,8 @@ SIGNATURES = {
     "attn_decode_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "attn_decode_chunk_len": (_i, [_i, _i, _i]),
     "attn_reserve_workspace": (_i, [_i, _i, _i, _i, _i]),
+    "attn_reserve_workspace_bytes": (_i, [_sz]),
+    "attn_debug_set_wait_limit": (_i, [ctypes.c_longlong]),
     "attn_device_status": (_i, [_vp, ctypes.POINTER(ctypes.c_uint)]),
     "attn_status_string": (ctypes.c_char_p, [_i]),
     "attn_version": (_i, []),

@@ -4,6 +4,7 @@
 #include "gqa_attn.h"
 #include "internal.h"
 
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -11,6 +12,13 @@
 
 // Per-device status word written by the kernels (bits ATTN_DEV_*).
 __device__ unsigned int g_attn_status;
+
+namespace {
+// Bound on each pipeline wait, in SM clock cycles (about 2 s at 2 GHz), passed to every launch;
+// attn_debug_set_wait_limit changes it for later launches.
+constexpr long long kDefaultWaitLimit = 4000000000LL;
+std::atomic<long long> g_wait_limit{kDefaultWaitLimit};
+}  // namespace
 
 namespace {
 
@@ -152,42 +160,80 @@ int sm_count(int *out)
     return ATTN_OK;
 }
 
-// Largest fp16 copy of V a prefill call makes in the library-owned scratch; larger calls convert
-// V on chip instead.
+// Largest fp16 copy of V a prefill call makes in its scratch; larger calls convert V on chip
+// instead.
 constexpr size_t kMaxV16Bytes = size_t(1) << 30;
 
-// Scratch for one tensor-core prefill call: the key split's partial results (split_bytes; 0 =
-// no split) followed, 256-byte aligned, by the fp16 copy of V (v16_bytes). Sets a.vpre, a.v16,
-// a.ws_o / a.ws_lse and a.J (kept only if its partials fit). If the scratch cannot grow now
-// (stream capture) the call runs without what does not fit: no split, and V converted on chip.
-int prefill_scratch(PrefillTcArgs &a, int J, size_t split_bytes, size_t v16_bytes,
-                    cudaStream_t st)
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Scratch of one tensor-core prefill call, in this order, each part 256-byte aligned: the V
+// scale area (per-slab exponents, then the conversion blocks' maxima; always needed), the key
+// split's partial results (0 = no split) and the fp16 copy of V (0 = V is converted on chip).
+struct PrefillScratch {
+    size_t nbg = 0, gx = 0;
+    size_t small = 0, split = 0, v16 = 0;
+    size_t split_blocks = 0;
+};
+
+PrefillScratch prefill_scratch_sizes(int B, int Hkv, int rows, int D, int sms, size_t split_bytes)
 {
-    const size_t off = (split_bytes + 255) & ~(size_t)255;
-    const bool want_v16 = v16_bytes <= kMaxV16Bytes;
-    void *ws = nullptr;
-    int rc = ATTN_ERR_WORKSPACE;
-    bool split = J > 0, v16 = want_v16;
-    if (split && v16) rc = workspace_acquire(off + v16_bytes, st, true, &ws);
-    if (rc == ATTN_ERR_WORKSPACE && v16) {
-        split = false;
-        rc = workspace_acquire(v16_bytes, st, true, &ws);
+    int gx = 1, gy = 1;
+    gqa::prefill_conv_grid(B * Hkv, rows, D, sms, &gx, &gy);
+    PrefillScratch p;
+    p.nbg = (size_t)B * Hkv;
+    p.gx = (size_t)gx;
+    p.small = align256(p.nbg * sizeof(int)) + align256(p.nbg * p.gx * sizeof(unsigned));
+    p.split = align256(split_bytes);
+    p.split_blocks = split_bytes / ((size_t)256 * (D + 1) * sizeof(float));
+    const size_t v16 = p.nbg * (size_t)rows * D * 2;
+    p.v16 = v16 <= kMaxV16Bytes ? v16 : 0;
+    return p;
+}
+
+// Places one call's scratch, trying in turn: split + fp16 copy, the copy alone, neither (V
+// converted on chip; the split needs the copy). It goes in the caller's workspace when one is
+// given (the first arrangement that fits), else in the library-owned buffer, grown when that is
+// possible (not during stream capture). Sets a.J, a.ws_o / a.ws_lse, a.vpre / a.v16 and
+// a.vexp / a.vmax. ATTN_ERR_WORKSPACE when not even the V scale area fits.
+int prefill_scratch(PrefillTcArgs &a, int J, const PrefillScratch &p, void *caller,
+                    size_t caller_bytes, cudaStream_t st)
+{
+    struct Option {
+        bool split, v16;
+    };
+    const Option opts[3] = {{true, true}, {false, true}, {false, false}};
+    for (const Option &o : opts) {
+        if (o.split && (J == 0 || p.split == 0)) continue;
+        if (o.v16 && p.v16 == 0) continue;
+        const size_t need = p.small + (o.split ? p.split : 0) + (o.v16 ? p.v16 : 0);
+        void *ws = nullptr;
+        if (caller != nullptr) {
+            if (caller_bytes < need) continue;
+            ws = caller;
+        } else {
+            const int rc = workspace_acquire(need, st, true, &ws);
+            if (rc == ATTN_ERR_WORKSPACE) continue;
+            if (rc != ATTN_OK) return rc;
+        }
+        uint8_t *base = static_cast<uint8_t *>(ws);
+        a.vexp = reinterpret_cast<int *>(base);
+        a.vmax = reinterpret_cast<unsigned *>(base + align256(p.nbg * sizeof(int)));
+        size_t off = p.small;
+        a.J = 0;
+        a.vpre = 0;
+        if (o.split) {
+            a.J = J;
+            a.ws_o = reinterpret_cast<float *>(base + off);
+            a.ws_lse = a.ws_o + p.split_blocks * 256 * a.D;
+            off += p.split;
+        }
+        if (o.v16) {
+            a.vpre = 1;
+            a.v16 = base + off;
+        }
+        return ATTN_OK;
     }
-    if (rc != ATTN_OK && rc != ATTN_ERR_WORKSPACE) return rc;
-    if (rc == ATTN_ERR_WORKSPACE) split = v16 = false;
-    a.J = 0;
-    a.vpre = 0;
-    if (split) {
-        const size_t blocks = split_bytes / ((size_t)256 * (a.D + 1) * sizeof(float));
-        a.J = J;
-        a.ws_o = static_cast<float *>(ws);
-        a.ws_lse = a.ws_o + blocks * 256 * a.D;
-    }
-    if (v16) {
-        a.vpre = 1;
-        a.v16 = static_cast<uint8_t *>(ws) + (split ? off : 0);
-    }
-    return ATTN_OK;
+    return ATTN_ERR_WORKSPACE;
 }
 
 int check_prefill(const void *q, const void *k, const void *v, void *o, float *lse, int B,
@@ -227,10 +273,12 @@ int check_decode(const void *q, const void *kc, const void *vc, const int *seqle
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
 
-// bf16 prefill on the tensor-core kernel for checked arguments and strides.
+// bf16 prefill on the tensor-core kernel for checked arguments and strides; scratch in `ws`
+// (ws_bytes) or, with ws == nullptr, in the library-owned buffer.
 int prefill_bf16(const void *q, const void *k, const void *v, void *o, float *lse, int B, int S,
                  int Hq, int Hkv, int D, float scale, int causal, int out_dtype, const Strides &qs,
-                 const Strides &ks, const Strides &vs, const Strides &os, void *stream)
+                 const Strides &ks, const Strides &vs, const Strides &os, void *ws,
+                 size_t ws_bytes, void *stream)
 {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     PrefillTcArgs a;
@@ -253,25 +301,23 @@ int prefill_bf16(const void *q, const void *k, const void *v, void *o, float *ls
     int rc = status_ptr(&a.status);
     if (rc != ATTN_OK) return rc;
     // Small grids (fewer row blocks x heads than SMs) split the keys of each row block over
-    // several blocks and merge; the partials use the library-owned scratch, as does the fp16
-    // copy of V.
+    // several blocks and merge; the partials use the scratch, as does the fp16 copy of V.
     int sms = 0;
     rc = sm_count(&sms);
     if (rc != ATTN_OK) return rc;
     a.sms = sms;
     int J = 0;
     const size_t need = gqa::prefill_split_plan(B, S, Hq, D, causal ? 1 : 0, sms, &J);
-    rc = prefill_scratch(a, J, need, (size_t)B * Hkv * S * D * 2, st);
+    rc = prefill_scratch(a, J, prefill_scratch_sizes(B, Hkv, S, D, sms, need), ws, ws_bytes, st);
     if (rc != ATTN_OK) return rc;
-    if (a.vpre) {
-        a.v_src = v;
-        a.v_sb = vs.b;
-        a.v_ss = vs.s;
-        a.v_sh = vs.h;
-        a.v_rows = S;
-        if (!encode_bf16_4d(&a.tv, a.v16, D, S, Hkv, B, contiguous(Hkv, S, D), true))
-            return ATTN_ERR_CUDA;
-    }
+    a.v_src = v;
+    a.v_sb = vs.b;
+    a.v_ss = vs.s;
+    a.v_sh = vs.h;
+    a.v_rows = S;
+    if (a.vpre &&
+        !encode_bf16_4d(&a.tv, a.v16, D, S, Hkv, B, contiguous(Hkv, S, D), true))
+        return ATTN_ERR_CUDA;
     return cuda_status(gqa::launch_prefill_tc(a, out_dtype == ATTN_F32, st));
 }
 
@@ -279,6 +325,7 @@ int prefill_bf16(const void *q, const void *k, const void *v, void *o, float *ls
 
 namespace gqa {
 int status_word_ptr(unsigned **out) { return status_ptr(out); }
+long long wait_limit_cycles() { return g_wait_limit.load(); }
 }  // namespace gqa
 
 extern "C" {
@@ -292,7 +339,7 @@ const char *attn_status_string(int s)
     case ATTN_ERR_INVALID: return "invalid argument";
     case ATTN_ERR_UNSUPPORTED: return "unsupported shape or dtype";
     case ATTN_ERR_ALIGN: return "pointer not 16-byte aligned";
-    case ATTN_ERR_WORKSPACE: return "decode workspace too small";
+    case ATTN_ERR_WORKSPACE: return "workspace too small";
     case ATTN_ERR_CUDA: return "CUDA error";
     case ATTN_ERR_TIMEOUT: return "device wait timed out";
     default: return "unknown status";
@@ -313,7 +360,32 @@ int attn_prefill_ex(const void *q, const void *k, const void *v, void *o, float 
             causal ? 1 : 0, st));
     return prefill_bf16(q, k, v, o, lse, B, S, Hq, Hkv, D, scale, causal, out_dtype,
                         contiguous(Hq, S, D), contiguous(Hkv, S, D), contiguous(Hkv, S, D),
-                        contiguous(Hq, S, D), stream);
+                        contiguous(Hq, S, D), nullptr, 0, stream);
+}
+
+size_t attn_prefill_workspace_bytes(int B, int S, int Hq, int Hkv, int D, int causal)
+{
+    if (B <= 0 || S <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || (D != 64 && D != 128))
+        return 0;
+    int sms = 0;
+    if (sm_count(&sms) != ATTN_OK) return 0;
+    int J = 0;
+    const size_t split = gqa::prefill_split_plan(B, S, Hq, D, causal ? 1 : 0, sms, &J);
+    const PrefillScratch p = prefill_scratch_sizes(B, Hkv, S, D, sms, split);
+    return p.small + (J > 0 && p.v16 > 0 ? p.split : 0) + p.v16;
+}
+
+int attn_prefill_ws(const void *q, const void *k, const void *v, void *o, float *lse, int B, int S,
+                    int Hq, int Hkv, int D, float scale, int causal, int out_dtype,
+                    void *workspace, size_t workspace_bytes, void *stream)
+{
+    int rc = check_prefill(q, k, v, o, lse, B, S, Hq, Hkv, D, scale, ATTN_BF16, out_dtype);
+    if (rc != ATTN_OK) return rc;
+    if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return ATTN_ERR_ALIGN;
+    return prefill_bf16(q, k, v, o, lse, B, S, Hq, Hkv, D, scale, causal, out_dtype,
+                        contiguous(Hq, S, D), contiguous(Hkv, S, D), contiguous(Hkv, S, D),
+                        contiguous(Hq, S, D), workspace, workspace_bytes, stream);
 }
 
 int attn_prefill_strided(const void *q, const void *k, const void *v, void *o, float *lse, int B,
@@ -333,7 +405,7 @@ int attn_prefill_strided(const void *q, const void *k, const void *v, void *o, f
         !strides_ok(os, out_dtype == ATTN_F32 ? 4 : 2))
         return ATTN_ERR_ALIGN;
     return prefill_bf16(q, k, v, o, lse, B, S, Hq, Hkv, D, scale, causal, out_dtype, qs, ks, vs,
-                        os, stream);
+                        os, nullptr, 0, stream);
 }
 
 namespace {
@@ -450,17 +522,16 @@ int chunk_or_varlen(const void *q, const void *kcache, const void *vcache, const
     if (rc != ATTN_OK) return rc;
     a.sms = sms;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    rc = prefill_scratch(a, 0, 0, (size_t)B * Hkv * max_len * D * 2, st);
+    rc = prefill_scratch(a, 0, prefill_scratch_sizes(B, Hkv, max_len, D, sms, 0), nullptr, 0, st);
     if (rc != ATTN_OK) return rc;
-    if (a.vpre) {
-        a.v_src = vcache;
-        a.v_sb = vs.b;
-        a.v_ss = vs.s;
-        a.v_sh = vs.h;
-        a.v_rows = max_len;
-        if (!encode_bf16_4d(&a.tv, a.v16, D, max_len, Hkv, B, contiguous(Hkv, max_len, D), true))
-            return ATTN_ERR_CUDA;
-    }
+    a.v_src = vcache;
+    a.v_sb = vs.b;
+    a.v_ss = vs.s;
+    a.v_sh = vs.h;
+    a.v_rows = max_len;
+    if (a.vpre &&
+        !encode_bf16_4d(&a.tv, a.v16, D, max_len, Hkv, B, contiguous(Hkv, max_len, D), true))
+        return ATTN_ERR_CUDA;
     return cuda_status(gqa::launch_prefill_tc(a, out_dtype == ATTN_F32,
                                               static_cast<cudaStream_t>(stream)));
 }
@@ -493,6 +564,12 @@ int attn_reserve_workspace(int B, int Hq, int Hkv, int D, int max_len)
     if (need == 0) return ATTN_ERR_INVALID;
     void *p = nullptr;
     return workspace_acquire(need, nullptr, true, &p);
+}
+
+int attn_reserve_workspace_bytes(size_t bytes)
+{
+    void *p = nullptr;
+    return workspace_acquire(bytes, nullptr, true, &p);
 }
 
 int attn_decode_ex(const void *q, const void *kcache, const void *vcache, const int *seqlens,
@@ -588,6 +665,12 @@ int attn_decode(const void *q, const void *kcache, const void *vcache, const int
 {
     return attn_decode_ex(q, kcache, vcache, seqlens, o, nullptr, B, Hq, Hkv, D, max_len, scale,
                           nullptr, 0, ATTN_BF16, stream);
+}
+
+int attn_debug_set_wait_limit(long long cycles)
+{
+    g_wait_limit.store(cycles > 0 ? cycles : kDefaultWaitLimit);
+    return ATTN_OK;
 }
 
 int attn_device_status(void *stream, unsigned int *status)

@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(kWarps * 32)
                         const __nv_bfloat16 *__restrict__ vc, const int *__restrict__ seqlens,
                         float *__restrict__ ws_o, float2 *__restrict__ ws_ml, int Hq, int Hkv,
                         int max_len, int chunk, int nsplit, float scale_log2,
-                        unsigned *__restrict__ status)
+                        unsigned *__restrict__ status, long long wait_limit)
 {
     using P = Plan<D, HG>;
     constexpr int LPK = P::LPK, GPW = P::GPW, T = P::T, NV = P::NV, SK = P::SK;
@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     int it = 0;
     for (int i = warp; i < nstage; i += kWarps, ++it) {
         const int slot = it % kRing;
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars[warp * kRing + slot], (it / kRing) & 1, &never));
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars[warp * kRing + slot], (it / kRing) & 1, &never, wait_limit));
         if (!ok) break;
         const uint8_t *stage = ring + (warp * kRing + slot) * P::STAGE;
         const int k0 = start + i * SK;
@@ -386,7 +386,8 @@ __global__ void __launch_bounds__(kWarps * 32)
         if (lane == 0) atomicOr(status, 2u);
         for (int r = 0; r < kRing; ++r) {
             const int i2 = warp + (it + r) * kWarps;
-            if (i2 < nstage) mbar_wait(&bars[warp * kRing + (it + r) % kRing], ((it + r) / kRing) & 1, &never);
+            if (i2 < nstage)
+                mbar_wait_drain(&bars[warp * kRing + (it + r) % kRing], ((it + r) / kRing) & 1);
         }
     }
 
@@ -498,7 +499,7 @@ __global__ void __launch_bounds__(kWarps * 32)
                          const __nv_bfloat16 *__restrict__ vc, const int *__restrict__ seqlens,
                          float *__restrict__ ws_o, float2 *__restrict__ ws_ml, int B, int Hq,
                          int Hkv, int max_len, float scale_log2, unsigned *__restrict__ status,
-                         RopeIn rope)
+                         RopeIn rope, long long wait_limit)
 {
     using P = Plan<D, HG>;
     constexpr int LPK = P::LPK, GPW = P::GPW, T = P::T, NV = P::NV, SK = P::SK;
@@ -639,7 +640,7 @@ __global__ void __launch_bounds__(kWarps * 32)
             }
             const int slot = it % kRing;
             ok = __all_sync(0xffffffffu,
-                            mbar_wait(&bars[warp * kRing + slot], (it / kRing) & 1, &never));
+                            mbar_wait(&bars[warp * kRing + slot], (it / kRing) & 1, &never, wait_limit));
             if (!ok) break;
             if constexpr (ROPE) {
                 if (cc.off + n == cc.Lb) {  // the stage holds the newest key, as its row n - 1
@@ -702,9 +703,10 @@ __global__ void __launch_bounds__(kWarps * 32)
             ++it;
         }
         if (!ok) {
+            // let every copy this warp started land before it leaves the shared memory
             if (lane == 0) atomicOr(status, 2u);
             for (int r = it; r < issued; ++r)
-                mbar_wait(&bars[warp * kRing + r % kRing], (r / kRing) & 1, &never);
+                mbar_wait_drain(&bars[warp * kRing + r % kRing], (r / kRing) & 1);
         }
     }
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -957,7 +959,8 @@ cudaError_t launch_split_t(const DecodeArgs &a, cudaStream_t st)
     return launch_pdl(decode_split_kernel<D, HG, QT>, grid, dim3(kWarps * 32), P::SMEM, st,
                       static_cast<const QT *>(a.q), static_cast<const __nv_bfloat16 *>(a.kc),
                       static_cast<const __nv_bfloat16 *>(a.vc), a.seqlens, a.ws_o, a.ws_ml,
-                      a.Hq, a.Hkv, a.max_len, a.chunk, a.nsplit, a.scale_log2, a.status);
+                      a.Hq, a.Hkv, a.max_len, a.chunk, a.nsplit, a.scale_log2, a.status,
+                      wait_limit_cycles());
 }
 
 int largest_group(int G)
@@ -993,8 +996,12 @@ cudaError_t launch_stream_t(const DecodeArgs &a, bool out_f32, cudaStream_t st)
             attr_set[dev] = true;
         }
     }
+    if (a.max_warps > 0 && blocks * kWarps > a.max_warps) blocks = a.max_warps / kWarps;
+    if (blocks < 1) return cudaErrorInvalidValue;
+    // partials: one row of D per (piece, head) for the warps actually launched (at most
+    // kStreamMaxWarps, which decode_workspace_bytes assumes), then one float2 per row
     float *ws_o = static_cast<float *>(a.ws);
-    const size_t rows = (size_t)kStreamMaxWarps * HG + (size_t)a.B * a.Hq;
+    const size_t rows = (size_t)blocks * kWarps * HG + (size_t)a.B * a.Hq;
     float2 *ws_ml = reinterpret_cast<float2 *>(ws_o + rows * D);
     RopeIn rope = {};
     if (ROPE) {
@@ -1008,7 +1015,7 @@ cudaError_t launch_stream_t(const DecodeArgs &a, bool out_f32, cudaStream_t st)
     e = launch_pdl(kern, dim3(blocks), dim3(kWarps * 32), P::RING + P::PBUF + P::BARS, st,
                    static_cast<const __nv_bfloat16 *>(a.q), static_cast<const __nv_bfloat16 *>(a.kc),
                    static_cast<const __nv_bfloat16 *>(a.vc), a.seqlens, ws_o, ws_ml, a.B, a.Hq,
-                   a.Hkv, a.max_len, a.scale_log2, a.status, rope);
+                   a.Hkv, a.max_len, a.scale_log2, a.status, rope, wait_limit_cycles());
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     const bool many = (long long)a.B * a.Hkv * (a.Hq / a.Hkv / HG) >= 128;  // streams
@@ -1115,6 +1122,21 @@ size_t decode_workspace_bytes(int B, int Hq, int Hkv, int D, int max_len)
     const size_t nsplit = ((size_t)max_len + chunk - 1) / chunk;
     const size_t rows = (size_t)B * Hq * nsplit;
     return rows * D * sizeof(float) + rows * sizeof(float2);
+}
+
+int decode_warps_within(int B, int Hq, int Hkv, int D, int max_len, size_t bytes)
+{
+    const size_t row = (size_t)D * sizeof(float) + sizeof(float2);
+    if (B > kStreamMaxBatch)
+        return decode_workspace_bytes(B, Hq, Hkv, D, max_len) <= bytes ? kStreamMaxWarps : 0;
+    const size_t HG = (size_t)largest_group(Hq / Hkv);
+    const size_t rows = bytes / row;
+    const size_t fixed = (size_t)B * Hq;
+    if (rows <= fixed) return 0;
+    size_t warps = (rows - fixed) / HG;
+    if (warps > (size_t)kStreamMaxWarps) warps = kStreamMaxWarps;
+    warps -= warps % kWarps;
+    return (int)warps;
 }
 
 cudaError_t launch_decode(const DecodeArgs &a0, bool out_f32, cudaStream_t st)

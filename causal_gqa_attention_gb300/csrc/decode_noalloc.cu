@@ -11,7 +11,8 @@
 // unnormalised output per query head) to scratch memory, and the merge kernel reads them back.
 // Here that scratch is g_noalloc_scratch below: a file-scope device array of
 // ATTN_DECODE_NOALLOC_SCRATCH_BYTES bytes that every GPU loading the library holds until the
-// process exits. Shapes whose partials do not fit are rejected.
+// process exits. For batches up to 1024 the split kernel runs on as many warps as the array has
+// room for; shapes that do not fit even so are rejected.
 //
 // Host code cannot use the array's name as a device pointer, so the first call on each device
 // looks its address up with cudaGetSymbolAddress (with that device current) and keeps it.
@@ -66,8 +67,11 @@ extern "C" int attn_decode_noalloc(const void *q, const void *kcache, const void
         return ATTN_ERR_ALIGN;
     if (!aligned4(seqlens) || (lse && !aligned4(lse))) return ATTN_ERR_ALIGN;
 
-    const size_t need = gqa::decode_workspace_bytes(B, Hq, Hkv, D, max_len);
-    if (need > (size_t)ATTN_DECODE_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_WORKSPACE;
+    // The stream kernel's partials grow with its warp count: launch only as many warps as the
+    // array has room for (the chunked kernel for large batches needs its full size).
+    const int warps = gqa::decode_warps_within(B, Hq, Hkv, D, max_len,
+                                               (size_t)ATTN_DECODE_NOALLOC_SCRATCH_BYTES);
+    if (warps <= 0) return ATTN_ERR_WORKSPACE;
 
     void *ws = nullptr;
     int rc = scratch_address(&ws);
@@ -87,6 +91,7 @@ extern "C" int attn_decode_noalloc(const void *q, const void *kcache, const void
     // Nothing needs clearing: every partial result the merge kernel reads was written by the
     // split kernel of the same call.
     a.ws = ws;
+    a.max_warps = warps;
     a.scale_log2 = scale * 1.4426950408889634f;
     rc = gqa::status_word_ptr(&a.status);
     if (rc != ATTN_OK) return rc;

@@ -12,7 +12,7 @@ namespace gqa {
 // q as a 4-D bf16 tensor {D, S, Hq, B} and k, v as {D, rows, Hkv, B} (rows = S, or max_kv for a
 // cache), each with its own strides, 64 x 128-row boxes and 128-byte swizzle.
 struct PrefillTcArgs {
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv;  // tv: the fp16 copy of V (vpre != 0) or V itself (bf16)
     void *o;        // bf16 or fp32, element (b, h, i, d) at o + b o_sb + i o_ss + h o_sh + d
     long long o_sb, o_ss, o_sh;
     float *lse;     // [B, Hq, S] or nullptr
@@ -32,15 +32,21 @@ struct PrefillTcArgs {
     float *ws_o = nullptr;    // [blocks, 256, D] fp32
     float *ws_lse = nullptr;  // [blocks, 256] fp32
     // vpre != 0: V is first converted to a contiguous fp16 copy v16 [B, Hkv, v_rows, D] (from
-    // v_src, element (b, g, r, d) at v_src + b v_sb + r v_ss + g v_sh + d) and tv maps that copy
-    // as fp16; vpre == 0: tv maps the bf16 V and the kernel converts on chip. Required with J.
+    // v_src, element (b, g, r, d) at v_src + b v_sb + r v_ss + g v_sh + d) and tv maps that
+    // copy; vpre == 0: tv maps the bf16 V and the kernel converts it on chip. Required with J.
     int vpre = 0;
     const void *v_src = nullptr;
     long long v_sb = 0, v_ss = 0, v_sh = 0;
     void *v16 = nullptr;
     int v_rows = 0;
     int sms = 0;  // SM count (sizes the conversion grid)
+    // V scale per (b, kv head) slab, always required: vmax holds the conversion blocks' maxima
+    // ([B * Hkv, gx] of prefill_conv_grid), vexp the chosen exponents [B * Hkv]
+    unsigned *vmax = nullptr;
+    int *vexp = nullptr;
 };
+// Grid (gx, gy) of the V conversion kernel for nbg (b, kv head) slabs of `rows` rows.
+void prefill_conv_grid(int nbg, int rows, int D, int sms, int *gx, int *gy);
 cudaError_t launch_prefill_tc(const PrefillTcArgs &a, bool out_f32, cudaStream_t stream);
 // Chooses the key split for a prefill shape on num_sms SMs: writes J (0 = no split) and returns
 // the workspace bytes it needs.
@@ -70,6 +76,9 @@ struct DecodeArgs {
     // q is then the unrotated bf16 query. nullptr: plain decode.
     const void *k_new = nullptr, *v_new = nullptr;
     const float *cos_t = nullptr, *sin_t = nullptr;
+    // at most this many warps for the stream kernel (0: as many as fit on the device); the
+    // partials' layout follows the warps actually launched
+    int max_warps = 0;
     // filled in by launch_decode for the chunked kernel
     float *ws_o = nullptr;
     float2 *ws_ml = nullptr;
@@ -88,11 +97,19 @@ cudaError_t launch_rope_append(const void *q, const void *k_new, const void *v_n
                                const int *seqlens, float *q_rot, int B, int Hq, int Hkv, int D,
                                int max_len, cudaStream_t stream);
 
+// Bound on each pipeline wait of the kernels launched from now on, in SM clock cycles: the
+// default (about 2 s) unless attn_debug_set_wait_limit lowered it. Passed as a kernel argument.
+long long wait_limit_cycles();
+
 // Device address of the library's status word on the current device.
 int status_word_ptr(unsigned **out);
 
 // Decode work split, shared by the workspace query and the launch.
 int decode_chunk_len(int B, int Hkv, int max_len);
 size_t decode_workspace_bytes(int B, int Hq, int Hkv, int D, int max_len);
+// Most stream-kernel warps whose partials fit in `bytes` of workspace (a multiple of the block's
+// warp count, at most the full grid), or for batches above the stream kernel's limit the full
+// grid if the chunked kernel's partials fit; 0 if nothing fits.
+int decode_warps_within(int B, int Hq, int Hkv, int D, int max_len, size_t bytes);
 
 }  // namespace gqa

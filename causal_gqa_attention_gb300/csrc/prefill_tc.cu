@@ -26,14 +26,22 @@
 // it. With bf16 (8-bit significand) a peaky softmax (a few keys carrying most of the weight)
 // showed errors near 8e-3 in the output; fp16 (11-bit significand) brings that to about 1e-3.
 // The tensor core needs both operands of one product in the same type, so V is converted to
-// fp16; that is exact for every bf16 value with 2^-14 <= |v| <= 65280. Normally a separate
-// HBM-bound kernel (convert_v_kernel) writes an fp16 copy of V once per call and the attention
-// kernel streams that: every V tile is read by many blocks (all heads of its group, all later
-// row blocks), and converting it in shared memory in each of them cost more than the copy. The
-// conversion also competed with the scores MMAs for shared-memory bandwidth (the tensor core
-// wins), which made it the slowest stage of the pipeline. When no scratch is available for the
-// copy (stream capture before the scratch has grown) warps 2-3 convert each landed tile in
-// place instead; both ways give the same fp16 values.
+// fp16. fp16 spans only 2^-14 .. 65504 with full precision, so every (batch, kv head) slab of V
+// gets a power-of-two scale 2^-e chosen from its largest finite |v|: e = 0 while that maximum
+// lies in [2^-9, 2^16) (every bf16 value there converts exactly, or with an error far below the
+// output's rounding), otherwise e puts the maximum in [2^14, 2^15), which keeps every value
+// within 2^28 of the maximum exact. O is linear in V, so the epilogue multiplies by 2^e and the
+// result is the same as with unscaled V, for any finite bf16 V. Normally a separate HBM-bound
+// kernel (convert_v_kernel) writes an fp16 copy of V once per call, with e = 0, and records each
+// block's maximum per slab; v_scale_kernel (one block per slab) picks e and rewrites the rare
+// slabs that need e != 0; the attention kernel streams the copy and reads e only for its
+// epilogue. Every V tile is read by many blocks (all heads of its group, all later row blocks),
+// and converting it in shared memory in each of them cost more than the copy; the conversion
+// also competed with the scores MMAs for shared-memory bandwidth (the tensor core wins), which
+// made it the slowest stage of the pipeline. When no scratch is available for the copy (stream
+// capture before the scratch has grown that far; a copy above 1 GiB) warps 2-3 convert each
+// landed tile in place instead, with the slab's scale from the same two small kernels; both ways
+// give the same fp16 values.
 //
 // The two tiles alternate on the tensor core: while tile 0's softmax runs, the tensor core
 // computes tile 1's P V and next S, and the other way round. Issue order per key tile j:
@@ -159,10 +167,52 @@ __host__ __device__ __forceinline__ int split_slots(int S, int causal, int J)
     return a > b ? a : b;
 }
 
-// 1 if either bf16 half of w has magnitude >= 2^16 (beyond the fp16 range) or is inf/NaN.
-__device__ __forceinline__ uint32_t too_big_for_f16(uint32_t w)
+// Largest finite magnitude among the bf16 halves of the four words of c, folded into `acc` as
+// two 16-bit lanes of magnitude bits (inf and NaN count as 0: no scale can bring them into the
+// fp16 range, and they propagate as they would in fp32).
+__device__ __forceinline__ uint32_t absmax_acc(uint32_t acc, uint4 c)
 {
-    return (uint32_t)((w & 0x7FFF0000u) >= 0x47800000u) | (uint32_t)((w & 0x7FFFu) >= 0x4780u);
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const uint32_t a = w[e] & 0x7FFF7FFFu;
+        acc = __vmaxu2(acc, a & __vcmpltu2(a, 0x7F807F80u));
+    }
+    return acc;
+}
+
+// Exponent e of a V slab's scale from its largest finite |v| (bf16 magnitude bits m): 0 while
+// the maximum lies in [2^-9, 2^16), else the e that puts it in [2^14, 2^15), within [-126, 113]
+// so that 2^e and 2^-e are normal fp32 numbers.
+__host__ __device__ __forceinline__ int v_scale_exponent(uint32_t m)
+{
+    if (m == 0) return 0;
+    int E;
+    if (m >= 0x80u) {
+        E = (int)((m >> 7) & 0xFFu) - 127;
+    } else {  // bf16 subnormal: m * 2^-133
+        int top = 0;
+        while ((m >> (top + 1)) != 0) ++top;
+        E = top - 133;
+    }
+    if (E >= -9 && E <= 15) return 0;
+    const int e = E - 14;
+    return e < -126 ? -126 : e;
+}
+
+// 2^e as an fp32 number, e in [-126, 127].
+__device__ __forceinline__ float exp2i(int e) { return __int_as_float((127 + e) << 23); }
+
+// Two bf16 (one 32-bit word) -> two fp16 of (value * s), round to nearest even. s is a power of
+// two that keeps every finite value of the slab within the fp16 range, so nothing saturates.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float s)
+{
+    return pack_f16x2(bf16lo(w) * s, bf16hi(w) * s);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w)
+{
+    return pack_f16x2(bf16lo(w), bf16hi(w));
 }
 
 // Zeroes rows >= rows_ok of a 128-row bf16 tile of nchunk 16-byte chunks (64-column boxes of
@@ -184,6 +234,9 @@ __device__ __noinline__ void zero_v_tail(uint4 *tile, int ct, int rows_ok, int n
 // prefill_split_merge_kernel combines the segments of each row.
 // VPRE = true: tv maps an fp16 copy of V written by convert_v_kernel (warps 2-3 have nothing to
 // do). VPRE = false: tv maps the bf16 V, converted on chip by warps 2-3.
+// vexp[b * Hkv + g]: the exponent e of V slab (b, g)'s scale (V is used as v * 2^-e, so O is
+// multiplied by 2^e), written by convert_v_kernel, which this grid depends on (programmatic
+// dependent launch): every thread that reads it first waits for that grid.
 template <int HD, bool OUT_F32, bool SPLIT, bool VPRE>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -191,7 +244,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                       float *__restrict__ lse, int B, int S, int Hq, int Hkv, float scale_log2,
                       int causal, unsigned *__restrict__ status, int J, float *__restrict__ ws_o,
                       float *__restrict__ ws_lse, const int *__restrict__ kv_lens, int max_kv,
-                      int front, long long o_sb, long long o_ss, long long o_sh, int NS)
+                      int front, long long o_sb, long long o_ss, long long o_sh, int NS,
+                      const int *__restrict__ vexp, long long wait_limit)
 {
     using G = Geo<HD>;
     constexpr uint32_t kTile = G::kTile, kOffQ = G::kOffQ, kOffK = G::kOffK, kOffV = G::kOffV,
@@ -298,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // K_jj and V_jj reuse the stages of K_jj-2 and V_jj-3, both last read by the
                 // MMAs of step jj - 2
                 if (jj >= 2 &&
-                    !mbar_wait(&bar[B_STEP + ((jj - 2) & 1)], ((jj - 2) >> 1) & 1, abort_flag))
+                    !mbar_wait(&bar[B_STEP + ((jj - 2) & 1)], ((jj - 2) >> 1) & 1, abort_flag, wait_limit))
                     break;
                 const int sk = jj % KST, uk = jj / KST;
                 mbar_arrive_expect_tx(&bar[B_KFULL + sk], kTile);
@@ -319,12 +373,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (*abort_flag) {
                 // let every copy this block started land before the block exits
-                volatile int never = 0;
-                mbar_wait(&bar[B_Q], 0, &never);
+                mbar_wait_drain(&bar[B_Q], 0);
                 for (int s = 0; s < KST; ++s)
-                    if (issued_k[s]) mbar_wait(&bar[B_KFULL + s], (issued_k[s] - 1) & 1, &never);
+                    if (issued_k[s]) mbar_wait_drain(&bar[B_KFULL + s], (issued_k[s] - 1) & 1);
                 for (int s = 0; s < VST; ++s)
-                    if (issued_v[s]) mbar_wait(&bar[B_VFULL + s], (issued_v[s] - 1) & 1, &never);
+                    if (issued_v[s]) mbar_wait_drain(&bar[B_VFULL + s], (issued_v[s] - 1) & 1);
             }
         }
     } else if (warp == 1) {
@@ -336,22 +389,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sQ = smem_u32(smem + kOffQ);
         const uint32_t sK = smem_u32(smem + kOffK);
         const uint32_t sV = smem_u32(smem + kOffV);
-        bool ok = __all_sync(FULL, mbar_wait(&bar[B_Q], 0, abort_flag));
+        bool ok = __all_sync(FULL, mbar_wait(&bar[B_Q], 0, abort_flag, wait_limit));
         for (int jj = 0; ok && jj <= nJ; ++jj) {
             const int j = jb + jj;
             const bool do_s = jj < nJ;
             const bool do_pv = jj >= 1;
             if (do_s &&
-                !__all_sync(FULL, mbar_wait(&bar[B_KFULL + jj % KST], (jj / KST) & 1, abort_flag)))
+                !__all_sync(FULL, mbar_wait(&bar[B_KFULL + jj % KST], (jj / KST) & 1, abort_flag, wait_limit)))
                 break;
             const int vbar = (VPRE ? B_VFULL : B_VREADY) + (jj - 1) % VST;  // V_jj-1 usable
             if (do_pv &&
-                !__all_sync(FULL, mbar_wait(&bar[vbar], ((jj - 1) / VST) & 1, abort_flag)))
+                !__all_sync(FULL, mbar_wait(&bar[vbar], ((jj - 1) / VST) & 1, abort_flag, wait_limit)))
                 break;
             tc_fence_after();
             for (int t = 0; t < 2 && ok; ++t) {
                 if (do_pv && j - 1 <= hi[t]) {
-                    if (!__all_sync(FULL, mbar_wait(&bar[B_PFULL + t], (jj - 1) & 1, abort_flag))) {
+                    if (!__all_sync(FULL, mbar_wait(&bar[B_PFULL + t], (jj - 1) & 1, abort_flag, wait_limit))) {
                         ok = false;
                         break;
                     }
@@ -385,18 +438,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // drain: all issued tcgen05 work finishes before TMEM is released
         mma_commit_warp(&bar[B_DRAIN]);
-        volatile int never = 0;
-        mbar_wait(&bar[B_DRAIN], 0, &never);
+        mbar_wait_drain(&bar[B_DRAIN], 0);
         __syncwarp();
     } else if (!VPRE && (warp == 2 || warp == 3)) {
         // ================================================================ V bf16 -> fp16
         // The P V product runs in fp16 (10-bit mantissa for P instead of bf16's 7): each V tile
-        // is converted in place once it lands, then handed to the tensor core.
+        // is converted in place, with the slab's scale, once it lands, then handed to the tensor
+        // core.
         const int ct = threadIdx.x - 64;
-        uint32_t over = 0;
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        const float vsc = exp2i(-vexp[b * Hkv + g]);  // this slab's scale 2^-e
         for (int jj = 0; jj < nJ; ++jj) {
             const int s = jj % VST;
-            if (!__all_sync(0xffffffffu, mbar_wait(&bar[B_VFULL + s], (jj / VST) & 1, abort_flag)))
+            if (!__all_sync(0xffffffffu, mbar_wait(&bar[B_VFULL + s], (jj / VST) & 1, abort_flag, wait_limit)))
                 break;
             uint4 *tile = reinterpret_cast<uint4 *>(smem + kOffV + s * kTile);
             // rows at or past L (a cache's stale rows may hold anything) become 0 first: p is
@@ -407,19 +461,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 4
             for (int c = ct; c < (int)(kTile / 16); c += 64) {
                 uint4 w = tile[c];
-                // |bf16| >= 2^16 (magnitude bits >= 0x4780) does not fit fp16; inf, NaN too
-                over |= too_big_for_f16(w.x) | too_big_for_f16(w.y) | too_big_for_f16(w.z) |
-                        too_big_for_f16(w.w);
-                w.x = bf16x2_to_f16x2_sat(w.x);
-                w.y = bf16x2_to_f16x2_sat(w.y);
-                w.z = bf16x2_to_f16x2_sat(w.z);
-                w.w = bf16x2_to_f16x2_sat(w.w);
+                w.x = bf16x2_to_f16x2_scaled(w.x, vsc);
+                w.y = bf16x2_to_f16x2_scaled(w.y, vsc);
+                w.z = bf16x2_to_f16x2_scaled(w.z, vsc);
+                w.w = bf16x2_to_f16x2_scaled(w.w, vsc);
                 tile[c] = w;
             }
             fence_proxy_async_smem();
             mbar_arrive(&bar[B_VREADY + s]);
         }
-        if (over) atomicOr(status, 4u);
     }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
@@ -436,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int j = jb; j <= hi[t]; ++j) {
                 const int jj = j - jb;
-                ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_SFULL + t], jj & 1, abort_flag));
+                ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_SFULL + t], jj & 1, abort_flag, wait_limit));
                 if (!ok) break;
                 tc_fence_after();
                 uint32_t sv[128];  // raw fp32 bits of the row's scores
@@ -515,15 +565,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const bool active = hi[t] >= jb;  // warp-uniform
             if (ok && active)
-                ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_OFULL + t], 0, abort_flag));
+                ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_OFULL + t], 0, abort_flag, wait_limit));
             // a row block whose keys fit in one segment writes its final result directly
             const bool direct = SPLIT && rb_segments(rb, S, causal, J) == 1;
+            // V was used as v * 2^-e: O comes out multiplied by 2^e
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            const float osc = exp2i(vexp[b * Hkv + g]);
             if (ok && SPLIT && !direct) {
                 // segment result: normalised O (fp32) and LSE in log2 units; an empty segment
                 // (this tile has no key tile in it) writes O = 0 and LSE = -inf
                 if (active) tc_fence_after();
                 const bool live = i < S;
-                const float inv = (active && l > 0.f) ? 1.f / l : 0.f;
+                const float inv = (active && l > 0.f) ? osc / l : 0.f;
                 const size_t prow = (size_t)blockIdx.x * (2 * BM) + t * BM + r;
 #pragma unroll 1
                 for (int c = 0; c < HD / 32; ++c) {
@@ -544,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // an inactive tile (its rows see no key) writes O = 0 and LSE = -inf
                 if (active) tc_fence_after();
                 const bool live = i < S;
-                const float inv = (active && l > 0.f) ? 1.f / l : 0.f;
+                const float inv = (active && l > 0.f) ? osc / l : 0.f;
                 const size_t orow = ((size_t)b * Hq + h) * S + (live ? i : 0);
                 const long long obase = b * o_sb + h * o_sh + (long long)(live ? i : 0) * o_ss;
 #pragma unroll 1
@@ -679,21 +732,25 @@ __global__ void __launch_bounds__(256)
 }
 
 // V (bf16, element (b, g, r, d) at v + b sb + r ss + g sh + d) -> a contiguous fp16 copy
-// [B, Hkv, rows, HD] for the P V product, saturating like the on-chip conversion (status bit 4
-// when a value does not fit). With kv_lens, rows at or past a sequence's key count are written
-// as 0 up to the end of their 128-row key tile (the attention kernel reads whole tiles, and
-// 0 * NaN from a stale cache row would not be 0); later tiles are never read and are skipped.
-// Grid: x blocks stride over one (b, g) slab, y over the slabs.
-template <int HD>
+// [B, Hkv, rows, HD] for the P V product (WRITE = true; WRITE = false only measures, for the
+// on-chip conversion). The copy is made with scale 1, which is exact for the usual range of V;
+// each block also records the largest finite |v| it saw in each (b, g) slab,
+// vmax[(b * Hkv + g) * gridDim.x + blockIdx.x] (bf16 magnitude bits), from which
+// v_scale_kernel picks the slab's scale and redoes the slabs that need another one.
+// With kv_lens, rows at or past a sequence's key count are written as 0 up to the end of their
+// 128-row key tile (the attention kernel reads whole tiles, and 0 * NaN from a stale cache row
+// would not be 0) and do not count towards the maximum; later tiles are never read and are
+// skipped. Grid: x blocks stride over one (b, g) slab, y over the slabs.
+template <int HD, bool WRITE>
 __global__ void __launch_bounds__(256)
     convert_v_kernel(const __nv_bfloat16 *__restrict__ v, long long sb, long long ss,
                      long long sh, uint4 *__restrict__ v16, int B, int Hkv, int rows,
-                     const int *__restrict__ kv_lens, int max_kv, unsigned *__restrict__ status)
+                     const int *__restrict__ kv_lens, int max_kv, unsigned *__restrict__ vmax)
 {
     constexpr int CPR = HD / 8;  // 16-byte chunks per row
     constexpr int LOG = HD == 128 ? 4 : 3;
+    __shared__ uint32_t red[8];
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    uint32_t over = 0;
     const int nbg = B * Hkv;
     for (int bg = blockIdx.y; bg < nbg; bg += gridDim.y) {
         const int b = bg / Hkv, g = bg - b * Hkv;
@@ -705,6 +762,7 @@ __global__ void __launch_bounds__(256)
         const long long lim = (long long)min((L + 127) & ~127, rows) * CPR;
         const __nv_bfloat16 *src = v + b * sb + g * sh;
         uint4 *dst = v16 + (long long)bg * rows * CPR;
+        uint32_t acc = 0;
         for (long long i = blockIdx.x * 256LL + threadIdx.x; i < lim;
              i += (long long)gridDim.x * 256) {
             const long long r = i >> LOG;
@@ -712,37 +770,148 @@ __global__ void __launch_bounds__(256)
             uint4 w = make_uint4(0, 0, 0, 0);
             if (r < L) {
                 w = *reinterpret_cast<const uint4 *>(src + r * ss + c * 8);
-                over |= too_big_for_f16(w.x) | too_big_for_f16(w.y) | too_big_for_f16(w.z) |
-                        too_big_for_f16(w.w);
-                w.x = bf16x2_to_f16x2_sat(w.x);
-                w.y = bf16x2_to_f16x2_sat(w.y);
-                w.z = bf16x2_to_f16x2_sat(w.z);
-                w.w = bf16x2_to_f16x2_sat(w.w);
+                acc = absmax_acc(acc, w);
+                w.x = bf16x2_to_f16x2(w.x);
+                w.y = bf16x2_to_f16x2(w.y);
+                w.z = bf16x2_to_f16x2(w.z);
+                w.w = bf16x2_to_f16x2(w.w);
+            }
+            if (WRITE) dst[i] = w;
+        }
+        uint32_t m = max(acc & 0xFFFFu, acc >> 16);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+#pragma unroll
+            for (int w2 = 1; w2 < 8; ++w2) m = max(m, red[w2]);
+            vmax[(size_t)bg * gridDim.x + blockIdx.x] = m;
+        }
+        __syncthreads();
+    }
+}
+
+// Picks the scale 2^-e of V slab bg = blockIdx.x (+ multiples of gridDim.x) from the xconv block
+// maxima convert_v_kernel recorded, writes e to vexp[bg], and with `redo` converts a slab whose
+// e is not 0 again, as v * 2^-e, into the fp16 copy (that takes the whole block a while, but only
+// a V beyond the fp16 range needs it). One block per slab keeps the grid small: its blocks hold
+// their SMs while they wait for the conversion kernel (this grid is its programmatic
+// dependent), and the attention kernel, launched the same way after this one, needs those SMs.
+template <int HD>
+__global__ void __launch_bounds__(256)
+    v_scale_kernel(const __nv_bfloat16 *__restrict__ v, long long sb, long long ss, long long sh,
+                   uint4 *__restrict__ v16, int B, int Hkv, int rows,
+                   const int *__restrict__ kv_lens, int max_kv,
+                   const unsigned *__restrict__ vmax, int xconv, int *__restrict__ vexp,
+                   int redo)
+{
+    constexpr int CPR = HD / 8;
+    constexpr int LOG = HD == 128 ? 4 : 3;
+    __shared__ uint32_t red[8];
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int nbg = B * Hkv;
+    for (int bg = blockIdx.x; bg < nbg; bg += gridDim.x) {
+        uint32_t m = 0;
+        for (int t = threadIdx.x; t < xconv; t += 256) m = max(m, vmax[(size_t)bg * xconv + t]);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+        __syncthreads();
+#pragma unroll
+        for (int w2 = 0; w2 < 8; ++w2) m = max(m, red[w2]);
+        __syncthreads();
+        const int e = v_scale_exponent(m);
+        if (threadIdx.x == 0) vexp[bg] = e;
+        if (!redo || e == 0) continue;
+        const int b = bg / Hkv, g = bg - b * Hkv;
+        int L = rows;
+        if (kv_lens != nullptr) {
+            L = kv_lens[b];
+            L = L < 0 ? 0 : (L > max_kv ? max_kv : L);
+        }
+        const float s = exp2i(-e);
+        const long long lim = (long long)min((L + 127) & ~127, rows) * CPR;
+        const __nv_bfloat16 *src = v + b * sb + g * sh;
+        uint4 *dst = v16 + (long long)bg * rows * CPR;
+        for (long long i = threadIdx.x; i < lim; i += 256) {
+            const long long r = i >> LOG;
+            const int c = (int)(i & (CPR - 1));
+            uint4 w = make_uint4(0, 0, 0, 0);
+            if (r < L) {
+                w = *reinterpret_cast<const uint4 *>(src + r * ss + c * 8);
+                w.x = bf16x2_to_f16x2_scaled(w.x, s);
+                w.y = bf16x2_to_f16x2_scaled(w.y, s);
+                w.z = bf16x2_to_f16x2_scaled(w.z, s);
+                w.w = bf16x2_to_f16x2_scaled(w.w, s);
             }
             dst[i] = w;
         }
     }
-    if (__any_sync(0xffffffffu, over != 0) && (threadIdx.x & 31) == 0) atomicOr(status, 4u);
 }
 
-cudaError_t launch_convert_v(const PrefillTcArgs &a, cudaStream_t st)
+}  // namespace
+
+// Grid of the V conversion kernel for nbg slabs of `rows` rows of head dim D on `sms` SMs:
+// about 8 blocks of 256 threads per SM in all. v_scale_kernel reads its gx block maxima.
+void prefill_conv_grid(int nbg, int rows, int D, int sms, int *gx, int *gy)
 {
-    const int nbg = a.B * a.Hkv;
     const int y = nbg < 65535 ? nbg : 65535;
-    const long long per = ((long long)a.v_rows * (a.D / 8) + 255) / 256;  // blocks per slab
-    long long x = (8LL * a.sms + y - 1) / y;  // about 8 blocks of 256 threads per SM in all
+    const long long per = ((long long)rows * (D / 8) + 255) / 256;  // blocks per slab
+    long long x = (8LL * (sms > 0 ? sms : 1) + y - 1) / y;
     if (x > per) x = per;
     if (x < 1) x = 1;
-    const dim3 grid((unsigned)x, (unsigned)y);
+    *gx = (int)x;
+    *gy = y;
+}
+
+namespace {
+
+// The kernels before the attention kernel: the fp16 copy of V with scale 1 (without a copy, only
+// the maxima), then the per-slab scale (v_scale_kernel, a programmatic dependent of the first).
+// The attention kernel is launched as a programmatic dependent of v_scale_kernel.
+cudaError_t launch_v_prep(const PrefillTcArgs &a, cudaStream_t st)
+{
+    int gx = 1, gy = 1;
+    prefill_conv_grid(a.B * a.Hkv, a.v_rows, a.D, a.sms, &gx, &gy);
+    const dim3 grid((unsigned)gx, (unsigned)gy);
     const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(a.v_src);
     uint4 *dst = static_cast<uint4 *>(a.v16);
-    if (a.D == 128)
-        convert_v_kernel<128><<<grid, 256, 0, st>>>(src, a.v_sb, a.v_ss, a.v_sh, dst, a.B, a.Hkv,
-                                                    a.v_rows, a.kv_lens, a.max_kv, a.status);
-    else
-        convert_v_kernel<64><<<grid, 256, 0, st>>>(src, a.v_sb, a.v_ss, a.v_sh, dst, a.B, a.Hkv,
-                                                   a.v_rows, a.kv_lens, a.max_kv, a.status);
-    return cudaGetLastError();
+    if (a.D == 128) {
+        if (a.vpre)
+            convert_v_kernel<128, true><<<grid, 256, 0, st>>>(src, a.v_sb, a.v_ss, a.v_sh, dst,
+                                                              a.B, a.Hkv, a.v_rows, a.kv_lens,
+                                                              a.max_kv, a.vmax);
+        else
+            convert_v_kernel<128, false><<<grid, 256, 0, st>>>(src, a.v_sb, a.v_ss, a.v_sh, dst,
+                                                               a.B, a.Hkv, a.v_rows, a.kv_lens,
+                                                               a.max_kv, a.vmax);
+    } else {
+        if (a.vpre)
+            convert_v_kernel<64, true><<<grid, 256, 0, st>>>(src, a.v_sb, a.v_ss, a.v_sh, dst,
+                                                             a.B, a.Hkv, a.v_rows, a.kv_lens,
+                                                             a.max_kv, a.vmax);
+        else
+            convert_v_kernel<64, false><<<grid, 256, 0, st>>>(src, a.v_sb, a.v_ss, a.v_sh, dst,
+                                                              a.B, a.Hkv, a.v_rows, a.kv_lens,
+                                                              a.max_kv, a.vmax);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    const int nbg = a.B * a.Hkv;
+    cfg.gridDim = dim3((unsigned)(nbg < 65535 ? nbg : 65535));
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, a.D == 128 ? v_scale_kernel<128> : v_scale_kernel<64>, src,
+                              a.v_sb, a.v_ss, a.v_sh, dst, a.B, a.Hkv, a.v_rows, a.kv_lens,
+                              a.max_kv, (const unsigned *)a.vmax, gx, a.vexp, a.vpre);
 }
 
 template <int HD, bool OUT_F32, bool SPLIT, bool VPRE>
@@ -770,10 +939,8 @@ cudaError_t launch_t(const PrefillTcArgs &a, cudaStream_t st)
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
-    if (VPRE) {
-        e = launch_convert_v(a, st);
-        if (e != cudaSuccess) return e;
-    }
+    e = launch_v_prep(a, st);
+    if (e != cudaSuccess) return e;
     {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)blocks);
@@ -781,11 +948,12 @@ cudaError_t launch_t(const PrefillTcArgs &a, cudaStream_t st)
         cfg.dynamicSmemBytes = Geo<HD>::kSmem;
         cfg.stream = st;
         cfg.attrs = pdl;
-        cfg.numAttrs = VPRE ? 1 : 0;  // starts while the conversion kernel finishes
+        cfg.numAttrs = 1;  // starts while the V kernels finish
         e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<HD, OUT_F32, SPLIT, VPRE>, a.tq, a.tk,
                                a.tv, a.o, a.lse, a.B, a.S, a.Hq, a.Hkv, a.scale_log2, a.causal,
                                a.status, a.J, a.ws_o, a.ws_lse, a.kv_lens,
-                               a.kv_lens ? a.max_kv : a.S, a.front, a.o_sb, a.o_ss, a.o_sh, NS);
+                               a.kv_lens ? a.max_kv : a.S, a.front, a.o_sb, a.o_ss, a.o_sh, NS,
+                               (const int *)a.vexp, wait_limit_cycles());
     }
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess || !SPLIT) return e;

@@ -72,19 +72,36 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
 // hanging the GPU.
 constexpr long long kWaitLimitCycles = 4000000000LL;
 
-// Waits for the phase with the given parity to complete. Returns false if the wait ran out or
-// another role of the block already gave up (*abort != 0); on running out it sets *abort.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort)
+// Waits for the phase with the given parity to complete. Returns false if the wait ran out
+// (after `limit` cycles; the kernels take it as an argument, normally kWaitLimitCycles) or
+// another role of the block already gave up (*abort != 0); on running out it sets *abort. Under
+// a short bound (a test of this path) the thread polls instead of sleeping, so any wait that
+// misses its first probe gives up; the default bound never fires in a working pipeline.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                          long long limit)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    const uint32_t hint = limit > 1000000 ? 100000u : 0u;
+    while (true) {
+        if (mbar_try_wait_sleep(bar, parity, hint)) return true;
+        if (*abort) return false;
+        if (clock64() - t0 > limit) {
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
+// Bounded wait used when a block drains after giving up: it waits for copies it started itself,
+// which always land, so it ignores the abort flag; it still gives up after the wait limit.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
-        if (*abort) return false;
-        if (clock64() - t0 > kWaitLimitCycles) {
-            *abort = 1;
-            return false;
-        }
+        if (clock64() - t0 > kWaitLimitCycles) return false;
     }
 }
 

@@ -51,7 +51,7 @@ typedef enum {
     ATTN_ERR_INVALID = 1,     /* NULL pointer, non-positive size, Hq % Hkv != 0, bad dtype   */
     ATTN_ERR_UNSUPPORTED = 2, /* valid but not built: head dim or dtype combination          */
     ATTN_ERR_ALIGN = 3,       /* a tensor pointer is not 16-byte aligned                     */
-    ATTN_ERR_WORKSPACE = 4,   /* decode workspace too small (or cannot grow while capturing) */
+    ATTN_ERR_WORKSPACE = 4,   /* workspace too small (or cannot grow while capturing)        */
     ATTN_ERR_CUDA = 5,        /* a CUDA runtime or driver call failed                        */
     ATTN_ERR_TIMEOUT = 6      /* reported through attn_device_status: a device wait expired  */
 } attn_status;
@@ -61,9 +61,7 @@ typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype;
 
 /* Bits of the device status word (attn_device_status). */
 #define ATTN_DEV_SEQLEN_CLAMPED 0x1u /* decode: a seqlens[b] was < 0 or > max_len; clamped   */
-#define ATTN_DEV_WAIT_TIMEOUT 0x2u   /* prefill: a pipeline wait ran out; the block stopped  */
-#define ATTN_DEV_FP16_RANGE 0x4u     /* bf16 prefill: a V element beyond +-65280 (or inf/NaN) */
-                                     /* was saturated for the fp16 P V product               */
+#define ATTN_DEV_WAIT_TIMEOUT 0x2u   /* a pipeline wait ran out; the block stopped          */
 
 /*
  * attn_prefill -- causal or non-causal prefill, bf16 in, bf16 out.
@@ -76,15 +74,22 @@ typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype;
  * each row block is split over several thread blocks and a second kernel merges their results
  * by log-sum-exp weights.
  * Computes on tcgen05 tensor cores with fp32 accumulation and fp32 softmax state: Q K^T from
- * the bf16 inputs; P V with P rounded to fp16 and V converted bf16 -> fp16 (exact for
- * 2^-14 <= |v| <= 65280; larger |v| saturate and set ATTN_DEV_FP16_RANGE in the status word).
+ * the bf16 inputs; P V with P rounded to fp16 and V converted bf16 -> fp16. Each (batch, kv
+ * head) slab of V is scaled by a power of two 2^-e picked from its largest finite |v| (e = 0
+ * unless that maximum is below 2^-9 or at least 2^16), and O is multiplied back by 2^e, so
+ * every finite bf16 V gives the same result as unscaled arithmetic would. V must be finite:
+ * an inf or NaN in V reaches rows whose probability for that key is 0 as NaN.
  * The conversion normally writes an fp16 copy of V (B*Hkv*S*D*2 bytes) once per call, which
  * the attention kernel then streams.
- * Scratch: the split's partial results and the fp16 copy of V use the library-owned scratch
- * buffer of the device (grown with cudaMalloc on first use, outside stream capture; the
- * buffer is shared with the decode calls, so calls on different streams must be serialised).
- * A call that cannot have the scratch (stream capture before it has grown; a copy above 1 GiB)
- * runs unsplit and converts V on chip instead, with the same results.
+ * Scratch: a small V scale area (per slab: one int, plus one word per conversion block), the
+ * split's partial results and the fp16 copy of V use the library-owned scratch buffer of the
+ * device (grown with cudaMalloc on first use, outside stream capture; the buffer is shared with
+ * the decode calls, so calls on different streams must be serialised, or use attn_prefill_ws).
+ * A call that cannot have all of it (stream capture before the buffer has grown that far; a
+ * copy above 1 GiB) runs unsplit and converts V on chip instead, with the same results. During
+ * stream capture a buffer too small even for the V scale area (no earlier call of any kind on
+ * the device) returns ATTN_ERR_WORKSPACE: reserve attn_prefill_workspace_bytes(...) with
+ * attn_reserve_workspace_bytes, or make one call, before capturing.
  */
 int attn_prefill(const void *q, const void *k, const void *v, void *o, float *lse, int B, int S,
                  int Hq, int Hkv, int D, float scale, int causal, void *stream);
@@ -101,6 +106,31 @@ int attn_prefill(const void *q, const void *k, const void *v, void *o, float *ls
 int attn_prefill_ex(const void *q, const void *k, const void *v, void *o, float *lse, int B,
                     int S, int Hq, int Hkv, int D, float scale, int causal, int in_dtype,
                     int out_dtype, void *stream);
+
+/*
+ * attn_prefill_workspace_bytes -- bytes of scratch a bf16 prefill call of this shape uses on the
+ * current device (the key split depends on its SM count): the V scale area, the split's partial
+ * results when the shape is split, and the fp16 copy of V when it is at most 1 GiB. 0 for
+ * invalid arguments (including D not in {64, 128}).
+ */
+size_t attn_prefill_workspace_bytes(int B, int S, int Hq, int Hkv, int D, int causal);
+
+/*
+ * attn_prefill_ws -- attn_prefill_ex for bf16 inputs with a caller-owned workspace, so calls on
+ * different streams (each with its own workspace) may overlap. workspace: device memory,
+ * 256-byte aligned (else ATTN_ERR_ALIGN), of workspace_bytes bytes; NULL = the library-owned
+ * buffer, as attn_prefill. The call uses the first arrangement that fits: split + fp16 copy of
+ * V, the copy alone, or neither (V converted on chip), all with the same results; with less than
+ * the V scale area it returns ATTN_ERR_WORKSPACE and launches nothing. Nothing in the workspace
+ * needs initialising, and the call never allocates. Calls sharing one workspace must not
+ * overlap on the GPU.
+ *   out_dtype ATTN_BF16 or ATTN_F32. Other arguments, layouts and numerics as attn_prefill.
+ * Source: "Hand-written Triton decoder" (m.nlpx.cn/news/28229) section 3.3 (a split's partial
+ * results go to a buffer that is allocated once and reused, never allocated per call).
+ */
+int attn_prefill_ws(const void *q, const void *k, const void *v, void *o, float *lse, int B, int S,
+                    int Hq, int Hkv, int D, float scale, int causal, int out_dtype,
+                    void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * attn_prefill_strided -- attn_prefill for bf16 operands in any layout whose head dim is
@@ -233,9 +263,12 @@ int attn_decode_ex(const void *q, const void *kcache, const void *vcache, const 
  * device array of ATTN_DECODE_NOALLOC_SCRATCH_BYTES bytes inside the library, which every GPU
  * that loads the library keeps until the process exits.
  *   Arguments as attn_decode_ex, without workspace/workspace_bytes.
- *   Returns ATTN_ERR_WORKSPACE when the shape's partials need more than
- *   ATTN_DECODE_NOALLOC_SCRATCH_BYTES (attn_decode_workspace_bytes tells how much a shape
- *   needs); nothing is launched then.
+ *   Batches up to 1024: the key list is split over as many warps as the array has room for
+ *   (up to the full grid), so any shape with B * Hq up to about 8000 at D = 128 (about 15800 at
+ *   D = 64) runs; a grid smaller than the full one only lowers parallelism. Larger batches (the
+ *   chunked kernel): the shape's partials, attn_decode_workspace_bytes(...), must fit in the
+ *   array.
+ *   Otherwise it returns ATTN_ERR_WORKSPACE and launches nothing.
  *   The first call on each device looks up the array's device address (with that device
  *   current); make that first call before any stream capture.
  *   All calls on a device share the one array and it keeps the last call's contents: calls
@@ -286,6 +319,20 @@ int attn_decode_chunk_len(int B, int Hkv, int max_len);
  * before capturing attn_decode in a CUDA graph (a graph keeps the buffer it was captured with;
  * growing later allocates a new one and keeps the old). */
 int attn_reserve_workspace(int B, int Hq, int Hkv, int D, int max_len);
+
+/* Grow the library-owned scratch buffer of the current device (shared by prefill and decode) to
+ * at least `bytes`, e.g. attn_prefill_workspace_bytes(...) before capturing a prefill in a CUDA
+ * graph. Not during stream capture. Returns ATTN_OK or ATTN_ERR_CUDA. */
+int attn_reserve_workspace_bytes(size_t bytes);
+
+/* Debugging aid for the failure path: every pipeline wait of the prefill and decode kernels
+ * launched after this call gives up after `cycles` SM clock cycles instead of the default bound
+ * (about 2 s; cycles <= 0 restores it). The bound is an argument of each launch (a CUDA graph
+ * keeps the one it was captured with). A wait that runs out sets ATTN_DEV_WAIT_TIMEOUT, the block
+ * lets the copies and tensor-core work it started finish, and returns without writing its
+ * results. A bound of a few cycles makes a wait that is not satisfied at its first probe give up,
+ * which lets a test exercise that path without a fault. Process-wide; returns ATTN_OK. */
+int attn_debug_set_wait_limit(long long cycles);
 
 /* Synchronise `stream`, then read and clear the current device's status word into *status
  * (bits ATTN_DEV_*). Returns ATTN_OK, or ATTN_ERR_CUDA if the synchronisation failed. */

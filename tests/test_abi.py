@@ -152,3 +152,21 @@ def test_decode_split_plan(lib):
     c = lib.attn_decode_chunk_len(B, 2, 4096)
     assert lib.attn_decode_workspace_bytes(B, 8, 2, 128, 4096) == B * 8 * (4096 // c) * (128 * 4 + 8)
     assert lib.attn_decode_workspace_bytes(2, 3, 2, 128, 10) == 0
+
+
+@pytest.mark.parametrize("args,code", [
+    # q, k, v, o, lse, B, S, Hq, Hkv, D, scale, causal, out, ws, ws_bytes
+    ((A16, A16, A16, A16, None, 1, 8, 2, 1, 128, 0.1, 1, 1, A16 + 16, 1 << 20), 3),  # ws not 256-B aligned
+    ((A16, A16, A16, A16, None, 1, 8, 3, 2, 128, 0.1, 1, 1, A16, 1 << 20), 1),       # Hq % Hkv
+    ((A16, A16, A16, A16, None, 1, 8, 2, 1, 96, 0.1, 1, 1, A16, 1 << 20), 2),        # D = 96
+    ((A16, A16, A16, A16, None, 1, 8, 2, 1, 128, 0.1, 1, 5, A16, 1 << 20), 1),       # out dtype
+])
+def test_prefill_ws_rejects_on_host(lib, args, code):
+    assert lib.attn_prefill_ws(*args, None) == code
+
+
+def test_prefill_workspace_bytes_invalid(lib):
+    # invalid shapes return 0 before any device query
+    assert lib.attn_prefill_workspace_bytes(1, 8, 3, 2, 128, 1) == 0
+    assert lib.attn_prefill_workspace_bytes(1, 8, 2, 1, 96, 1) == 0
+    assert lib.attn_prefill_workspace_bytes(0, 8, 2, 1, 128, 1) == 0
