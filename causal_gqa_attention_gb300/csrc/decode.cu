@@ -149,8 +149,9 @@ __device__ __forceinline__ void stage_update(const uint8_t *stage, int nvalid, i
         pw[gl * NV + v] = make_float2(p, p);
     }
     __syncwarp();
-    // ---- O += P V for the group's keys. Rows past nvalid hold finite stale data (the ring is
-    // zeroed when the block starts and only ever receives cache rows) and get p = 0.
+    // ---- O += P V for the group's keys. V rows past nvalid are zero (the split kernel clears
+    // its ring at start, the stream kernel clears them before a partial stage's copy) and get
+    // p = 0.
 #pragma unroll
     for (int t = 0; t < T; ++t) {
         const uint4 w = *reinterpret_cast<const uint4 *>(stage + SK * P::ROW +
@@ -513,9 +514,6 @@ __global__ void __launch_bounds__(kWarps * 32)
     const int G = Hq / Hkv, SUB = G / HG, NGS = Hkv * SUB;
     const int W = blockIdx.x * kWarps + warp, NWT = gridDim.x * kWarps;
 
-    for (int i = threadIdx.x; i < P::RING / 16; i += kWarps * 32)
-        reinterpret_cast<uint4 *>(ring)[i] = make_uint4(0, 0, 0, 0);
-    fence_proxy_async_smem();
     if (threadIdx.x == 0) {
         for (int i = 0; i < kWarps * kRing; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
@@ -575,11 +573,19 @@ __global__ void __launch_bounds__(kWarps * 32)
             const long long left_piece = (long long)(pc.Lb - pc.off);
             const long long left_slice = r1 - pc.pos;
             const int n = (int)min((long long)SK, min(left_piece, left_slice));
+            const int slot = issued % kRing;
+            uint8_t *dst = ring + (warp * kRing + slot) * P::STAGE;
+            if (n < SK) {
+                // V rows past the copy get p = 0, and 0 * NaN would not be 0: zero them (the
+                // ring is not cleared at start, and a slot keeps an earlier stage's rows)
+                uint4 *vz = reinterpret_cast<uint4 *>(dst + (SK + n) * P::ROW);
+                for (int c = lane; c < (SK - n) * P::ROW / 16; c += 32) vz[c] = make_uint4(0, 0, 0, 0);
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
             if (lane == 0) {
                 const int g = pc.sl / SUB;
                 const size_t row = ((size_t)pc.b * Hkv + g) * (size_t)max_len + pc.off;
-                const int slot = issued % kRing;
-                uint8_t *dst = ring + (warp * kRing + slot) * P::STAGE;
                 uint64_t *bar = &bars[warp * kRing + slot];
                 mbar_arrive_expect_tx(bar, 2u * n * P::ROW);
                 bulk_load(dst, kc + row * D, n * P::ROW, bar);
@@ -735,7 +741,6 @@ __global__ void __launch_bounds__(MW * 32)
     const int G = Hq / Hkv, SUB = G / HG, NGS = Hkv * SUB;
     const int g = h / G, gs = (h % G) / HG, hl = (h % G) % HG;
     const int sl = g * SUB + gs;
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     const long long total = warp_len_sum(seqlens, B, max_len, lane) * NGS;
     const long long base = warp_len_sum(seqlens, b, max_len, lane) * NGS;
     const long long KP = stream_slice(total, nwt);
@@ -744,6 +749,11 @@ __global__ void __launch_bounds__(MW * 32)
     const int wf = (int)(start / KP);
     const int n = Lb > 0 ? (int)((start + Lb - 1) / KP) - wf + 1 : 0;
     const size_t row0 = ((size_t)wf + (size_t)b * NGS + sl) * HG + hl;  // piece j: row0 + j*HG
+    // Everything above reads only seqlens, which the stream kernel does not write: this grid is
+    // launched once every stream block has passed its own dependency wait, so whatever wrote
+    // seqlens before the stream kernel has finished. Only the partials need the wait, which
+    // now overlaps the stream kernel's tail instead of adding a round of loads after it.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     float M = -INFINITY, Ls = 0.f, acc[DL];
 #pragma unroll
@@ -835,12 +845,14 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
     constexpr int DL = D / 32;  // dims per lane
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int bh = blockIdx.x * kMergeWarps + warp;
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (bh >= BH) return;
     const int b = bh / Hq;
     int L = seqlens[b];
     L = L < 0 ? 0 : (L > max_len ? max_len : L);
     const int n = (L + chunk - 1) / chunk;
+    // seqlens is not written by the split kernel (launched after every split block passed its
+    // own dependency wait); only the chunk states need the wait
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const float2 *ml = ws_ml + (size_t)bh * nsplit;
     const float *po = ws_o + (size_t)bh * nsplit * D + lane * DL;
 
