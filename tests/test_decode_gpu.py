@@ -42,6 +42,14 @@ def test_decode_configured(name):
     _check(q, kc, vc, sl, name)
 
 
+@pytest.mark.parametrize("seed", [1, 2])
+def test_decode_batched_other_seeds(seed):
+    """The configured batched decode (B32, lengths U[256, 4096]) drawn from two more seeds."""
+    cfg = workloads.CONFIGS["c4b"]
+    q, kc, vc, sl = workloads.config_decode_inputs(cfg, seed=seed)
+    _check(q, kc, vc, sl, f"c4b seed {seed}")
+
+
 @pytest.mark.parametrize("B,Hq,Hkv,D,max_len,lens", [
     (4, 8, 2, 128, 300, [1, 31, 32, 33]),
     (3, 8, 2, 128, 4096, [255, 256, 4096]),
@@ -73,9 +81,9 @@ def test_decode_empty_sequence():
 
 
 def test_decode_caller_workspace_and_determinism():
-    """A caller workspace takes the separate merge kernel, the library's scratch the merge inside
-    the stream kernel (per-stream key counters, reset by the warp that completes a stream): both
-    agree with the oracle, and each gives identical bits on every call."""
+    """A caller workspace and the library-owned scratch run the same split and merge kernels:
+    both agree with the oracle, and each gives identical bits on every call (the merge combines
+    a stream's pieces in a fixed order)."""
     cga = library()
     dev = device()
     cfg = workloads.CONFIGS["c4b"]

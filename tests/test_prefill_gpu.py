@@ -76,6 +76,19 @@ def test_prefill_bf16_c3_full():
     check_out(o16, o_ref, "bf16", "c3 bf16 out")
 
 
+@pytest.mark.parametrize("seed", [1, 2])
+def test_prefill_bf16_c3_other_seeds(seed):
+    """The configured B1 Hq8 Hkv2 S2048 q x3 causal workload drawn from two more seeds."""
+    cfg = workloads.CONFIGS["c3"]
+    q, k, v = workloads.config_prefill_inputs(cfg, seed=seed)
+    o_ref, lse_ref = oracle.prefill(q, k, v, True, cfg.scale)
+    o32, lse = _run(q, k, v, True, torch.float32)
+    check_out(o32, o_ref, "bf16_pre", f"c3 seed {seed} fp32 out")
+    check_lse(lse, lse_ref, f"c3 seed {seed} lse")
+    o16, _ = _run(q, k, v, True, torch.bfloat16)
+    check_out(o16, o_ref, "bf16", f"c3 seed {seed} bf16 out")
+
+
 def test_prefill_bf16_c3_noncausal_and_other_seed():
     q, k, v = workloads.prefill_inputs(1, 8, 2, 2048, 128, "bf16", 3.0, seed=7)
     o_ref, lse_ref = oracle.prefill(q, k, v, False, 1 / math.sqrt(128))
@@ -87,16 +100,18 @@ def test_prefill_bf16_c3_noncausal_and_other_seed():
 @pytest.mark.parametrize("name", ["c5a", "c5b"])
 def test_prefill_bf16_long_context_sampled(name):
     """Configured long-context workloads at full size; rows sampled for the oracle (every 64th
-    row and the last 128 rows of every head)."""
+    row and the last 128 rows of every head). Both the bf16 output (after the final rounding) and
+    the fp32 output (before it, where the long rows' fp32 accumulation would show) are checked."""
     cfg = workloads.CONFIGS[name]
     q, k, v = workloads.config_prefill_inputs(cfg)
-    o16, lse = _run(q, k, v, True, torch.bfloat16)
     rows = sampled_rows(cfg.B, cfg.Hq, cfg.S)
     o_ref, lse_ref = oracle.prefill(q, k, v, True, cfg.scale, rows=rows)
-    o_rows = o16.reshape(-1, cfg.D)[torch.as_tensor(rows, device=o16.device)]
-    lse_rows = lse.reshape(-1)[torch.as_tensor(rows, device=lse.device)]
-    check_out(o_rows, o_ref, "bf16", f"{name} sampled rows")
-    check_lse(lse_rows, lse_ref, f"{name} sampled lse")
+    for out_dtype, kind in ((torch.bfloat16, "bf16"), (torch.float32, "bf16_pre")):
+        o, lse = _run(q, k, v, True, out_dtype)
+        idx = torch.as_tensor(rows, device=o.device)
+        check_out(o.reshape(-1, cfg.D)[idx], o_ref, kind, f"{name} sampled rows {kind}")
+        check_lse(lse.reshape(-1)[idx], lse_ref, f"{name} sampled lse {kind}")
+        del o, lse
 
 
 def test_prefill_deterministic():
