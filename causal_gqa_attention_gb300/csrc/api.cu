@@ -172,7 +172,7 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 struct PrefillScratch {
     size_t nbg = 0, gx = 0;
     size_t small = 0, split = 0, v16 = 0;
-    size_t split_blocks = 0;
+    size_t split_rows = 0;  // rows of partial results (blocks x rows per block)
 };
 
 PrefillScratch prefill_scratch_sizes(int B, int Hkv, int rows, int D, int sms, size_t split_bytes)
@@ -184,7 +184,7 @@ PrefillScratch prefill_scratch_sizes(int B, int Hkv, int rows, int D, int sms, s
     p.gx = (size_t)gx;
     p.small = align256(p.nbg * sizeof(int)) + align256(p.nbg * p.gx * sizeof(unsigned));
     p.split = align256(split_bytes);
-    p.split_blocks = split_bytes / ((size_t)256 * (D + 1) * sizeof(float));
+    p.split_rows = split_bytes / ((size_t)(D + 1) * sizeof(float));
     const size_t v16 = p.nbg * (size_t)rows * D * 2;
     p.v16 = v16 <= kMaxV16Bytes ? v16 : 0;
     return p;
@@ -224,7 +224,7 @@ int prefill_scratch(PrefillTcArgs &a, int J, const PrefillScratch &p, void *call
         if (o.split) {
             a.J = J;
             a.ws_o = reinterpret_cast<float *>(base + off);
-            a.ws_lse = a.ws_o + p.split_blocks * 256 * a.D;
+            a.ws_lse = a.ws_o + p.split_rows * a.D;
             off += p.split;
         }
         if (o.v16) {
@@ -306,8 +306,9 @@ int prefill_bf16(const void *q, const void *k, const void *v, void *o, float *ls
     rc = sm_count(&sms);
     if (rc != ATTN_OK) return rc;
     a.sms = sms;
-    int J = 0;
-    const size_t need = gqa::prefill_split_plan(B, S, Hq, D, causal ? 1 : 0, sms, &J);
+    int J = 0, pair = 0;
+    const size_t need = gqa::prefill_split_plan(B, S, Hq, D, causal ? 1 : 0, sms, &pair, &J);
+    a.pair = pair;
     rc = prefill_scratch(a, J, prefill_scratch_sizes(B, Hkv, S, D, sms, need), ws, ws_bytes, st);
     if (rc != ATTN_OK) return rc;
     a.v_src = v;
@@ -369,8 +370,8 @@ size_t attn_prefill_workspace_bytes(int B, int S, int Hq, int Hkv, int D, int ca
         return 0;
     int sms = 0;
     if (sm_count(&sms) != ATTN_OK) return 0;
-    int J = 0;
-    const size_t split = gqa::prefill_split_plan(B, S, Hq, D, causal ? 1 : 0, sms, &J);
+    int J = 0, pair = 0;
+    const size_t split = gqa::prefill_split_plan(B, S, Hq, D, causal ? 1 : 0, sms, &pair, &J);
     const PrefillScratch p = prefill_scratch_sizes(B, Hkv, S, D, sms, split);
     return p.small + (J > 0 && p.v16 > 0 ? p.split : 0) + p.v16;
 }

@@ -27,7 +27,10 @@ struct PrefillTcArgs {
     // with kv_lens: 0 = the queries are the last S tokens (cache chunk); 1 = the queries are
     // tokens 0..S-1 of a padded batch, kv_lens[b] of them valid (rows past it are padding)
     int front = 0;
-    // key split for small grids (0 = none): blocks of at most J key tiles, partials in ws
+    // small grids: pair != 0 gives each block 128 query rows, its two softmax warpgroups taking
+    // the key tiles in turns (combined in the block); J > 0 splits each row block's key tiles
+    // into segments of at most J tiles, one block each, partials in ws
+    int pair = 0;
     int J = 0;
     float *ws_o = nullptr;    // [blocks, 256, D] fp32
     float *ws_lse = nullptr;  // [blocks, 256] fp32
@@ -48,9 +51,9 @@ struct PrefillTcArgs {
 // Grid (gx, gy) of the V conversion kernel for nbg (b, kv head) slabs of `rows` rows.
 void prefill_conv_grid(int nbg, int rows, int D, int sms, int *gx, int *gy);
 cudaError_t launch_prefill_tc(const PrefillTcArgs &a, bool out_f32, cudaStream_t stream);
-// Chooses the key split for a prefill shape on num_sms SMs: writes J (0 = no split) and returns
-// the workspace bytes it needs.
-size_t prefill_split_plan(int B, int S, int Hq, int D, int causal, int num_sms, int *J);
+// Chooses the small-grid plan for a prefill shape on num_sms SMs: writes pair (0/1) and J
+// (0 = no split) and returns the workspace bytes the split needs.
+size_t prefill_split_plan(int B, int S, int Hq, int D, int causal, int num_sms, int *pair, int *J);
 
 // Prefill on CUDA cores in fp32 (fp32 q/k/v/o), head dim 64 or 128.
 cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, float *o,

@@ -124,7 +124,8 @@ enum : int {
     B_PFULL = B_SFULL + 2,      // 2 (per tile)
     B_OFULL = B_PFULL + 2,      // 2 (per tile)
     B_DRAIN = B_OFULL + 2,
-    NUM_BARS = B_DRAIN + 1
+    B_ML = B_DRAIN + 1,         // pair mode: both softmax warpgroups posted their (m, l)
+    NUM_BARS = B_ML + 1
 };
 static_assert(NUM_BARS * 8 + 8 <= 256, "barrier area");
 
@@ -139,14 +140,16 @@ __host__ __device__ __forceinline__ int last_key_tile(int causal, int q_first, i
     return lim < nkv - 1 ? lim : nkv - 1;
 }
 
-// Key tiles that the row block rb (rows 256 rb .. 256 rb + 255) visits.
-__host__ __device__ __forceinline__ int rb_key_tiles(int rb, int S, int causal)
+// Key tiles that the row block rb of `rows` rows (256, or 128 in pair mode) visits: every tile
+// up to the one holding its last row (causal), or all of them.
+__host__ __device__ __forceinline__ int rb_key_tiles(int rb, int S, int causal, int rows)
 {
     const int nkv = (S + BN - 1) / BN;
-    const int q0 = rb * 2 * BM;
-    const int l0 = last_key_tile(causal, q0, nkv);
-    const int l1 = (q0 + BM < S) ? last_key_tile(causal, q0 + BM, nkv) : -1;
-    return (l0 > l1 ? l0 : l1) + 1;
+    if (!causal) return nkv;
+    const int q0 = rb * rows;
+    const int qlast = (q0 + rows < S ? q0 + rows : S) - 1;
+    const int l = qlast / BN;
+    return (l < nkv - 1 ? l : nkv - 1) + 1;
 }
 
 // Split mode: row block rb is cut into ceil(tiles / J) segments of at most J key tiles, each
@@ -154,16 +157,16 @@ __host__ __device__ __forceinline__ int rb_key_tiles(int rb, int S, int causal)
 // block's segment count), so block -> (row block, segment, head) is plain arithmetic: blocks
 // are numbered heaviest row block first (row block n_rb - 1 - blockIdx / (NS * heads)), then
 // segment, then batch x head. Slots past a row block's segments exit at once.
-__host__ __device__ __forceinline__ int rb_segments(int rb, int S, int causal, int J)
+__host__ __device__ __forceinline__ int rb_segments(int rb, int S, int causal, int J, int rows)
 {
-    return (rb_key_tiles(rb, S, causal) + J - 1) / J;
+    return (rb_key_tiles(rb, S, causal, rows) + J - 1) / J;
 }
 
 // Segment slots per row block in split mode: the most segments any row block has.
-__host__ __device__ __forceinline__ int split_slots(int S, int causal, int J)
+__host__ __device__ __forceinline__ int split_slots(int S, int causal, int J, int rows)
 {
-    const int n_rb = (S + 2 * BM - 1) / (2 * BM);
-    const int a = rb_segments(n_rb - 1, S, causal, J), b = rb_segments(0, S, causal, J);
+    const int n_rb = (S + rows - 1) / rows;
+    const int a = rb_segments(n_rb - 1, S, causal, J, rows), b = rb_segments(0, S, causal, J, rows);
     return a > b ? a : b;
 }
 
@@ -237,7 +240,7 @@ __device__ __noinline__ void zero_v_tail(uint4 *tile, int ct, int rows_ok, int n
 // vexp[b * Hkv + g]: the exponent e of V slab (b, g)'s scale (V is used as v * 2^-e, so O is
 // multiplied by 2^e), written by convert_v_kernel, which this grid depends on (programmatic
 // dependent launch): every thread that reads it first waits for that grid.
-template <int HD, bool OUT_F32, bool SPLIT, bool VPRE>
+template <int HD, bool OUT_F32, bool SPLIT, bool VPRE, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, void *__restrict__ out,
@@ -261,7 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kSoftmaxWarp0 = 4;  // first of the 8 softmax warps
 
     // ---- work item: heaviest row blocks first (causal), heads of one group adjacent
-    const int n_rb = (S + 2 * BM - 1) / (2 * BM);
+    constexpr int RB = PAIR ? BM : 2 * BM;  // query rows per block
+    const int n_rb = (S + RB - 1) / RB;
     int rb, hb, seg = 0;
     if (!SPLIT) {
         rb = n_rb - 1 - (int)blockIdx.x / (Hq * B);
@@ -272,11 +276,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rem = (int)blockIdx.x % per_rb;
         seg = rem / (Hq * B);
         hb = rem % (Hq * B);
-        if (seg >= rb_segments(rb, S, causal, J)) return;  // empty slot: nothing set up yet
+        if (seg >= rb_segments(rb, S, causal, J, RB)) return;  // empty slot: nothing set up yet
     }
     const int h = hb % Hq, b = hb / Hq;
     const int g = h / (Hq / Hkv);
-    const int q0 = rb * 2 * BM;
+    const int q0 = rb * RB;
     // Keys: L of them. Plain prefill: L = S. Chunk against a cache (kv_lens given): the S
     // queries are the last S of the L_b cached tokens, so query row i sits at key position
     // i + off, off = L_b - S.
@@ -292,20 +296,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     // are padding that sees no key
     const int off = front ? 0 : L - S;
     const int nkv = (L + BN - 1) / BN;
-    const int n_tiles = (q0 + BM < S) ? 2 : 1;
+    // Q tiles loaded: two (rows q0.., q0 + 128..), or one in pair mode, where both softmax
+    // warpgroups work on the same 128 rows and take the block's key tiles in turns
+    const int n_tiles = (!PAIR && q0 + BM < S) ? 2 : 1;
     int last_j[2];
     last_j[0] = (front && q0 >= L) ? -1 : last_key_tile(causal, q0 + off, nkv);
-    last_j[1] = (n_tiles == 2 && !(front && q0 + BM >= L))
+    last_j[1] = (!PAIR && n_tiles == 2 && !(front && q0 + BM >= L))
                     ? last_key_tile(causal, q0 + BM + off, nkv)
                     : -1;
     const int n_j = max(last_j[0], last_j[1]) + 1;  // 0: no key at all (O = 0, LSE = -inf)
-    // key tiles [jb, je) of this block; tile t works on [jb, hi[t]] (empty when hi[t] < jb)
+    // key tiles [jb, je) of this block. Tile t (softmax warpgroup t) works on the tiles from
+    // first_j[t] to hi[t], every tile (two Q tiles) or every other one (pair mode: tile t takes
+    // jb + t, jb + t + 2, ...); it has none when hi[t] < first_j[t].
     const int jb = SPLIT ? seg * J : 0;
     const int je = SPLIT ? min(jb + J, n_j) : n_j;
     const int nJ = je - jb;
-    int hi[2];
-    hi[0] = min(je - 1, last_j[0]);
-    hi[1] = min(je - 1, last_j[1]);
+    int hi[2], first_j[2];
+    if (PAIR) {
+        for (int t = 0; t < 2; ++t) {
+            first_j[t] = jb + t;
+            const int last = je - 1;
+            hi[t] = (((last - jb) & 1) == t) ? last : last - 1;
+        }
+    } else {
+        first_j[0] = first_j[1] = jb;
+        hi[0] = min(je - 1, last_j[0]);
+        hi[1] = min(je - 1, last_j[1]);
+    }
 
     if (threadIdx.x == 0) {
         mbar_init(&bar[B_Q], 1);
@@ -321,6 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bar[B_OFULL + t], 1);
         }
         mbar_init(&bar[B_DRAIN], 1);
+        mbar_init(&bar[B_ML], 2 * BM);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -389,6 +407,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sQ = smem_u32(smem + kOffQ);
         const uint32_t sK = smem_u32(smem + kOffK);
         const uint32_t sV = smem_u32(smem + kOffV);
+        // O_t += P_t V_(jj-1): the P V of key tile jb + jj - 1 for tile t, its kp-th P
+        auto issue_pv = [&](int t, int jj, int kp) {
+            const uint32_t vbase = sV + ((jj - 1) % VST) * kTile;
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk) {
+                // B = V rows 16kk..16kk+15: MN-major, 64-col chunks 16 KB apart (one chunk when
+                // HD = 64), 8-row groups 1 KB apart
+                const uint64_t bd = smem_desc_sw128(vbase + kk * 2048, kBox, 1024);
+                mma_ts_warp(tmem + kColO + t * 128, tmem + kColS + t * 128 + kk * 8, bd, idO,
+                            (kp > 0 || kk > 0) ? 1u : 0u);
+            }
+            if (jb + jj - 1 == hi[t]) mma_commit_warp(&bar[B_OFULL + t]);
+        };
+        // S_t = Q K_jj^T (Q tile t, or the block's one Q tile in pair mode)
+        auto issue_s = [&](int t, int jj) {
+            const uint32_t qbase = sQ + (PAIR ? 0 : t) * kTile;
+            const uint32_t kbase = sK + (jj % KST) * kTile;
+#pragma unroll
+            for (int kk = 0; kk < HD / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+                const uint64_t ad = smem_desc_sw128(qbase + off, 16, 1024);
+                const uint64_t bd = smem_desc_sw128(kbase + off, 16, 1024);
+                mma_ss_warp(tmem + kColS + t * 128, ad, bd, idS, kk > 0 ? 1u : 0u);
+            }
+            mma_commit_warp(&bar[B_SFULL + t]);
+        };
         bool ok = __all_sync(FULL, mbar_wait(&bar[B_Q], 0, abort_flag, wait_limit));
         for (int jj = 0; ok && jj <= nJ; ++jj) {
             const int j = jb + jj;
@@ -398,42 +442,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                 !__all_sync(FULL, mbar_wait(&bar[B_KFULL + jj % KST], (jj / KST) & 1, abort_flag, wait_limit)))
                 break;
             const int vbar = (VPRE ? B_VFULL : B_VREADY) + (jj - 1) % VST;  // V_jj-1 usable
-            if (do_pv &&
-                !__all_sync(FULL, mbar_wait(&bar[vbar], ((jj - 1) / VST) & 1, abort_flag, wait_limit)))
-                break;
-            tc_fence_after();
-            for (int t = 0; t < 2 && ok; ++t) {
-                if (do_pv && j - 1 <= hi[t]) {
-                    if (!__all_sync(FULL, mbar_wait(&bar[B_PFULL + t], (jj - 1) & 1, abort_flag, wait_limit))) {
-                        ok = false;
+            if constexpr (PAIR) {
+                // Key tile j belongs to tile (j - jb) & 1. The scores go first: their tile's
+                // previous P was read by a P V issued in an earlier step (tcgen05 operations
+                // complete in order), so they need no P, and the other tile's softmax is not
+                // held up by this one's.
+                const int ts = jj & 1, tp = (jj - 1) & 1;
+                tc_fence_after();
+                if (do_s && j <= hi[ts]) issue_s(ts, jj);
+                if (do_pv && j - 1 <= hi[tp]) {
+                    const int kp = (jj - 1) >> 1;  // tile tp's P number
+                    if (!__all_sync(FULL, mbar_wait(&bar[vbar], ((jj - 1) / VST) & 1, abort_flag, wait_limit)) ||
+                        !__all_sync(FULL, mbar_wait(&bar[B_PFULL + tp], kp & 1, abort_flag, wait_limit)))
                         break;
-                    }
                     tc_fence_after();
-                    const uint32_t vbase = sV + ((jj - 1) % VST) * kTile;
-#pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk) {
-                        // B = V rows 16kk..16kk+15: MN-major, 64-col chunks 16 KB apart (one
-                        // chunk when HD = 64), 8-row groups 1 KB apart
-                        const uint64_t bd = smem_desc_sw128(vbase + kk * 2048, kBox, 1024);
-                        mma_ts_warp(tmem + kColO + t * 128, tmem + kColS + t * 128 + kk * 8, bd,
-                                    idO, (jj - 1 > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    if (j - 1 == hi[t]) mma_commit_warp(&bar[B_OFULL + t]);
+                    issue_pv(tp, jj, kp);
                 }
-                if (do_s && j <= hi[t]) {
-                    const uint32_t qbase = sQ + t * kTile;
-                    const uint32_t kbase = sK + (jj % KST) * kTile;
-#pragma unroll
-                    for (int kk = 0; kk < HD / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-                        const uint64_t ad = smem_desc_sw128(qbase + off, 16, 1024);
-                        const uint64_t bd = smem_desc_sw128(kbase + off, 16, 1024);
-                        mma_ss_warp(tmem + kColS + t * 128, ad, bd, idS, kk > 0 ? 1u : 0u);
+            } else {
+                if (do_pv &&
+                    !__all_sync(FULL, mbar_wait(&bar[vbar], ((jj - 1) / VST) & 1, abort_flag, wait_limit)))
+                    break;
+                tc_fence_after();
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (do_pv && j - 1 <= hi[t]) {
+                        if (!__all_sync(FULL, mbar_wait(&bar[B_PFULL + t], (jj - 1) & 1, abort_flag, wait_limit))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_pv(t, jj, jj - 1);
                     }
-                    mma_commit_warp(&bar[B_SFULL + t]);
+                    if (do_s && j <= hi[t]) issue_s(t, jj);
                 }
+                if (!ok) break;
             }
-            if (!ok) break;
             mma_commit_warp(&bar[B_STEP + (jj & 1)]);  // frees K_jj and V_jj-1
         }
         // drain: all issued tcgen05 work finishes before TMEM is released
@@ -477,15 +519,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = (warp - kSoftmaxWarp0) / 4;
         const int wq = warp & 3;
         const int r = wq * 32 + lane;  // row within the tile = TMEM lane
-        const int i = q0 + t * BM + r;  // query row
+        const int i = q0 + (PAIR ? 0 : t) * BM + r;  // query row
         const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
         const uint32_t tS = lane_base + kColS + t * 128;
         const uint32_t tO = lane_base + kColO + t * 128;
-        if (t < n_tiles) {
+        if (PAIR || t < n_tiles) {
             float m_ref = -INFINITY, l = 0.f;
             bool ok = true;
-            for (int j = jb; j <= hi[t]; ++j) {
-                const int jj = j - jb;
+            for (int j = first_j[t]; j <= hi[t]; j += PAIR ? 2 : 1) {
+                const int jj = PAIR ? (j - first_j[t]) >> 1 : j - jb;  // this tile's step number
                 ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_SFULL + t], jj & 1, abort_flag, wait_limit));
                 if (!ok) break;
                 tc_fence_after();
@@ -563,21 +605,97 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&bar[B_PFULL + t]);
                 m_ref = m_new;
             }
-            const bool active = hi[t] >= jb;  // warp-uniform
+            const bool active = hi[t] >= first_j[t];  // warp-uniform
             if (ok && active)
                 ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_OFULL + t], 0, abort_flag, wait_limit));
             // a row block whose keys fit in one segment writes its final result directly
-            const bool direct = SPLIT && rb_segments(rb, S, causal, J) == 1;
+            const bool direct = SPLIT && rb_segments(rb, S, causal, J, RB) == 1;
             // V was used as v * 2^-e: O comes out multiplied by 2^e
             asm volatile("griddepcontrol.wait;" ::: "memory");
             const float osc = exp2i(vexp[b * Hkv + g]);
-            if (ok && SPLIT && !direct) {
+            if constexpr (PAIR) {
+                // Both warpgroups hold (m, l, O) of the same rows over different key tiles. Each
+                // posts its (m, l) in the second Q buffer (never loaded in pair mode), then
+                // combines its half of the columns of both O accumulators with the weights
+                // 2^(m_t - M) and writes them (an empty segment or a row that sees no key: O = 0,
+                // LSE = -inf).
+                constexpr unsigned FULL = 0xffffffffu;
+                float *ml = reinterpret_cast<float *>(smem + kOffQ + kTile);
+                ml[(t * BM + r) * 2] = active ? m_ref : -INFINITY;
+                ml[(t * BM + r) * 2 + 1] = active ? l : 0.f;
+                mbar_arrive(&bar[B_ML]);
+                if (ok) ok = __all_sync(FULL, mbar_wait(&bar[B_ML], 0, abort_flag, wait_limit));
+                const int u = 1 - t;
+                const bool active_u = hi[u] >= first_j[u];
+                if (ok && active_u)
+                    ok = __all_sync(FULL, mbar_wait(&bar[B_OFULL + u], 0, abort_flag, wait_limit));
+                if (ok) {
+                    tc_fence_after();
+                    const float mt = active ? m_ref : -INFINITY, lt = active ? l : 0.f;
+                    const float mu = ml[(u * BM + r) * 2], lu = ml[(u * BM + r) * 2 + 1];
+                    const float M = fmaxf(mt, mu);
+                    const float Mz = (M == -INFINITY) ? 0.f : M;
+                    const float wt = active ? ex2(mt - Mz) : 0.f;
+                    const float wu = active_u ? ex2(mu - Mz) : 0.f;
+                    const float Ls = wt * lt + wu * lu;
+                    const float inv = Ls > 0.f ? osc / Ls : 0.f;
+                    const float ct = wt * inv, cu = wu * inv;
+                    const bool part = SPLIT && !direct;
+                    const bool live = i < S;
+                    const uint32_t tOu = lane_base + kColO + u * 128;
+                    const size_t prow = (size_t)blockIdx.x * RB + r;
+                    const long long obase = b * o_sb + h * o_sh + (long long)(live ? i : 0) * o_ss;
+#pragma unroll 1
+                    for (int c = t * (HD / 64); c < (t + 1) * (HD / 64); ++c) {
+                        uint32_t a[32], bu[32];
+                        if (active)
+                            tmem_ld32(tO + c * 32, a);
+                        else
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) a[e] = 0u;
+                        if (active_u)
+                            tmem_ld32(tOu + c * 32, bu);
+                        else
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) bu[e] = 0u;
+                        if (!live) continue;
+                        float x[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            x[e] = fmaf(ct, __uint_as_float(a[e]), cu * __uint_as_float(bu[e]));
+                        if (part || OUT_F32) {
+                            float4 *dst = reinterpret_cast<float4 *>(
+                                part ? ws_o + prow * HD + c * 32
+                                     : static_cast<float *>(out) + obase + c * 32);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                dst[e] = make_float4(x[4 * e], x[4 * e + 1], x[4 * e + 2], x[4 * e + 3]);
+                        } else {
+                            uint4 *dst = reinterpret_cast<uint4 *>(
+                                static_cast<__nv_bfloat16 *>(out) + obase + c * 32);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                dst[e] = make_uint4(pack_bf16x2(x[8 * e], x[8 * e + 1]),
+                                                    pack_bf16x2(x[8 * e + 2], x[8 * e + 3]),
+                                                    pack_bf16x2(x[8 * e + 4], x[8 * e + 5]),
+                                                    pack_bf16x2(x[8 * e + 6], x[8 * e + 7]));
+                        }
+                    }
+                    if (live && t == 0) {
+                        const float lse2 = Ls > 0.f ? M + log2f(Ls) : -INFINITY;
+                        if (part)
+                            ws_lse[prow] = lse2;  // log2 units
+                        else if (lse != nullptr)
+                            lse[((size_t)b * Hq + h) * S + i] = lse2 * 0.69314718055994531f;
+                    }
+                }
+            } else if (ok && SPLIT && !direct) {
                 // segment result: normalised O (fp32) and LSE in log2 units; an empty segment
                 // (this tile has no key tile in it) writes O = 0 and LSE = -inf
                 if (active) tc_fence_after();
                 const bool live = i < S;
                 const float inv = (active && l > 0.f) ? osc / l : 0.f;
-                const size_t prow = (size_t)blockIdx.x * (2 * BM) + t * BM + r;
+                const size_t prow = (size_t)blockIdx.x * RB + t * BM + r;
 #pragma unroll 1
                 for (int c = 0; c < HD / 32; ++c) {
                     uint32_t ov[32];
@@ -657,7 +775,7 @@ __global__ void __launch_bounds__(256)
     prefill_split_merge_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_lse,
                                void *__restrict__ out, float *__restrict__ lse, int B, int S,
                                int Hq, int causal, int J, long long o_sb, long long o_ss,
-                               long long o_sh, int NS)
+                               long long o_sh, int NS, int RB)
 {
     constexpr int DPL = HD / 32;  // dims per lane: 4 or 2
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -666,10 +784,10 @@ __global__ void __launch_bounds__(256)
     if (row >= (long long)B * Hq * S) return;
     const int i = (int)(row % S);
     const int hb = (int)(row / S);  // b * Hq + h
-    const int n_rb = (S + 2 * BM - 1) / (2 * BM);
-    const int rb = i / (2 * BM), rloc = i % (2 * BM);
+    const int n_rb = (S + RB - 1) / RB;
+    const int rb = i / RB, rloc = i % RB;
     const int first = (n_rb - 1 - rb) * NS * Hq * B;  // first block of row block rb
-    const int nseg = rb_segments(rb, S, causal, J);
+    const int nseg = rb_segments(rb, S, causal, J, RB);
     if (nseg == 1) return;  // that row block wrote its result itself
     // every load of the row in one round: segment LSEs and this lane's dims of each O
     float ls[8];
@@ -680,8 +798,8 @@ __global__ void __launch_bounds__(256)
         x[k] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (k < nseg) {
             const size_t item = (size_t)first + (size_t)k * Hq * B + hb;
-            ls[k] = ws_lse[item * (2 * BM) + rloc];
-            const float *src = ws_o + (item * (2 * BM) + rloc) * HD + lane * DPL;
+            ls[k] = ws_lse[item * RB + rloc];
+            const float *src = ws_o + (item * RB + rloc) * HD + lane * DPL;
             if constexpr (DPL == 4) {
                 x[k] = *reinterpret_cast<const float4 *>(src);
             } else {
@@ -914,27 +1032,28 @@ cudaError_t launch_v_prep(const PrefillTcArgs &a, cudaStream_t st)
                               a.max_kv, (const unsigned *)a.vmax, gx, a.vexp, a.vpre);
 }
 
-template <int HD, bool OUT_F32, bool SPLIT, bool VPRE>
+template <int HD, bool OUT_F32, bool SPLIT, bool VPRE, bool PAIR>
 cudaError_t launch_t(const PrefillTcArgs &a, cudaStream_t st)
 {
+    constexpr auto kern = prefill_tc_kernel<HD, OUT_F32, SPLIT, VPRE, PAIR>;
     static bool attr_set[64] = {};  // the attribute is set once per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 64 || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(prefill_tc_kernel<HD, OUT_F32, SPLIT, VPRE>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<HD>::kSmem);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<HD>::kSmem);
         if (e != cudaSuccess) return e;
         // the warpgroups' register split assumes exactly kRegsLaunch registers per thread
         cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<HD, OUT_F32, SPLIT, VPRE>);
+        e = cudaFuncGetAttributes(&fa, kern);
         if (e != cudaSuccess) return e;
         if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
         if (dev < 64) attr_set[dev] = true;
     }
-    const int n_rb = (a.S + 2 * BM - 1) / (2 * BM);
+    constexpr int RB = PAIR ? BM : 2 * BM;
+    const int n_rb = (a.S + RB - 1) / RB;
     long long blocks = (long long)n_rb * a.Hq * a.B;
-    const int NS = SPLIT ? split_slots(a.S, a.causal, a.J) : 1;
+    const int NS = SPLIT ? split_slots(a.S, a.causal, a.J, RB) : 1;
     if (SPLIT) blocks = (long long)n_rb * NS * a.Hq * a.B;
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -949,9 +1068,8 @@ cudaError_t launch_t(const PrefillTcArgs &a, cudaStream_t st)
         cfg.stream = st;
         cfg.attrs = pdl;
         cfg.numAttrs = 1;  // starts while the V kernels finish
-        e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<HD, OUT_F32, SPLIT, VPRE>, a.tq, a.tk,
-                               a.tv, a.o, a.lse, a.B, a.S, a.Hq, a.Hkv, a.scale_log2, a.causal,
-                               a.status, a.J, a.ws_o, a.ws_lse, a.kv_lens,
+        e = cudaLaunchKernelEx(&cfg, kern, a.tq, a.tk, a.tv, a.o, a.lse, a.B, a.S, a.Hq, a.Hkv,
+                               a.scale_log2, a.causal, a.status, a.J, a.ws_o, a.ws_lse, a.kv_lens,
                                a.kv_lens ? a.max_kv : a.S, a.front, a.o_sb, a.o_ss, a.o_sh, NS,
                                (const int *)a.vexp, wait_limit_cycles());
     }
@@ -966,21 +1084,27 @@ cudaError_t launch_t(const PrefillTcArgs &a, cudaStream_t st)
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, prefill_split_merge_kernel<HD, OUT_F32>, (const float *)a.ws_o,
                               (const float *)a.ws_lse, a.o, a.lse, a.B, a.S, a.Hq, a.causal, a.J,
-                              a.o_sb, a.o_ss, a.o_sh, NS);
+                              a.o_sb, a.o_ss, a.o_sh, NS, RB);
+}
+
+template <int HD, bool PAIR>
+cudaError_t launch_hp(const PrefillTcArgs &a, bool out_f32, cudaStream_t st)
+{
+    // the key split always has scratch, so it always has the fp16 copy of V as well
+    if (a.J > 0)
+        return out_f32 ? launch_t<HD, true, true, true, PAIR>(a, st)
+                       : launch_t<HD, false, true, true, PAIR>(a, st);
+    if (a.vpre)
+        return out_f32 ? launch_t<HD, true, false, true, PAIR>(a, st)
+                       : launch_t<HD, false, false, true, PAIR>(a, st);
+    return out_f32 ? launch_t<HD, true, false, false, PAIR>(a, st)
+                   : launch_t<HD, false, false, false, PAIR>(a, st);
 }
 
 template <int HD>
 cudaError_t launch_hd(const PrefillTcArgs &a, bool out_f32, cudaStream_t st)
 {
-    // the key split always has scratch, so it always has the fp16 copy of V as well
-    if (a.J > 0)
-        return out_f32 ? launch_t<HD, true, true, true>(a, st)
-                       : launch_t<HD, false, true, true>(a, st);
-    if (a.vpre)
-        return out_f32 ? launch_t<HD, true, false, true>(a, st)
-                       : launch_t<HD, false, false, true>(a, st);
-    return out_f32 ? launch_t<HD, true, false, false>(a, st)
-                   : launch_t<HD, false, false, false>(a, st);
+    return a.pair ? launch_hp<HD, true>(a, out_f32, st) : launch_hp<HD, false>(a, out_f32, st);
 }
 
 }  // namespace
@@ -992,8 +1116,10 @@ cudaError_t launch_prefill_tc(const PrefillTcArgs &a, bool out_f32, cudaStream_t
     return cudaErrorInvalidValue;
 }
 
-size_t prefill_split_plan(int B, int S, int Hq, int D, int causal, int num_sms, int *J_out)
+size_t prefill_split_plan(int B, int S, int Hq, int D, int causal, int num_sms, int *pair_out,
+                          int *J_out)
 {
+    constexpr int RB = 2 * BM;  // rows per block of the plain (two-tile) blocks
     // Splitting the key range of the long (causal: the late) row blocks into segments of J key
     // tiles evens out the blocks' work when the grid is only a few waves deep. The choice is an
     // estimate of the finishing time: blocks (one per SM at a time, heaviest first, as launched)
@@ -1002,8 +1128,19 @@ size_t prefill_split_plan(int B, int S, int Hq, int D, int causal, int num_sms, 
     // merge launch. Row blocks left in one segment write their result directly. At most 8
     // segments per row block (the merge kernel reads up to 8).
     *J_out = 0;
-    const int n_rb = (S + 2 * BM - 1) / (2 * BM);
+    *pair_out = 0;
+    const int n_rb = (S + RB - 1) / RB;
     const long long heads = (long long)Hq * B;
+    // A grid of two-tile blocks that fits in one wave of SMs: pair mode instead, 128 rows per
+    // block, whose two softmax warpgroups take the key tiles in turns (the heaviest row block's
+    // chain of key steps is cut in two inside the block, with no partials and no merge kernel).
+    // Measured at one wave or less it beats every key split (B1 S2048 25.6 vs 31.7 us, B1 S4096
+    // 42.0 vs 50.2, B2 S2048 31.7 vs 35.8); at two waves it loses (B1 S8192 126 vs 101), and
+    // pair blocks with a key split never won.
+    if (num_sms > 0 && (long long)n_rb * heads <= num_sms) {
+        *pair_out = 1;
+        return 0;
+    }
     if ((long long)n_rb * heads >= 4LL * num_sms || num_sms <= 0) return 0;
     static std::mutex mu;
     static std::map<std::array<long long, 6>, int> cache;
@@ -1024,7 +1161,7 @@ size_t prefill_split_plan(int B, int S, int Hq, int D, int causal, int num_sms, 
             constexpr double kMerge = 2.1;
             constexpr double kRowSteps = 1.05e-4;
             int nmax = 0;
-            for (int rb = 0; rb < n_rb; ++rb) nmax = std::max(nmax, rb_key_tiles(rb, S, causal));
+            for (int rb = 0; rb < n_rb; ++rb) nmax = std::max(nmax, rb_key_tiles(rb, S, causal, RB));
             std::vector<double> load;
             auto estimate = [&](int J) {
                 load.assign(num_sms, 0.0);
@@ -1032,7 +1169,7 @@ size_t prefill_split_plan(int B, int S, int Hq, int D, int causal, int num_sms, 
                     load.begin(), load.end());
                 double rows_split = 0.0;
                 for (int rb = n_rb - 1; rb >= 0; --rb) {
-                    const int t = rb_key_tiles(rb, S, causal);
+                    const int t = rb_key_tiles(rb, S, causal, RB);
                     const int ns = J > 0 ? (t + J - 1) / J : 1;
                     if (ns > 1) rows_split += 2.0 * BM * heads * ns;
                     for (int k = 0; k < ns; ++k) {
@@ -1067,8 +1204,8 @@ size_t prefill_split_plan(int B, int S, int Hq, int D, int causal, int num_sms, 
     }
     if (best == 0) return 0;
     *J_out = best;
-    const long long blocks = (long long)n_rb * split_slots(S, causal, best) * heads;
-    return (size_t)blocks * (2 * BM) * (D + 1) * sizeof(float);
+    const long long blocks = (long long)n_rb * split_slots(S, causal, best, RB) * heads;
+    return (size_t)blocks * RB * (D + 1) * sizeof(float);
 }
 
 }  // namespace gqa

@@ -28,7 +28,7 @@ D64 = [
     # B, Hq, Hkv, S, causal, q_mult
     (1, 1, 1, 1, True, 1.0), (1, 2, 1, 63, False, 1.0), (2, 4, 2, 129, True, 1.0),
     (1, 4, 1, 255, False, 3.0), (1, 12, 12, 512, True, 1.0), (1, 12, 12, 512, False, 1.0),
-    (2, 2, 1, 300, True, 3.0), (1, 8, 2, 2048, True, 3.0),   # the last two use the key split
+    (2, 2, 1, 300, True, 3.0), (1, 8, 2, 2048, True, 3.0),   # small grids: pair-mode blocks
 ]
 
 
@@ -97,7 +97,7 @@ def _bshd(t, dev):
 
 @pytest.mark.parametrize("B,Hq,Hkv,S,D,causal", [
     (2, 8, 2, 300, 128, True), (1, 4, 4, 1000, 128, False), (2, 8, 2, 700, 64, True),
-    (1, 8, 2, 2048, 128, True),   # key split: the merge kernel writes through the strides
+    (1, 8, 2, 2048, 128, True),   # pair-mode blocks write through the strides
 ])
 def test_prefill_bshd_layout(B, Hq, Hkv, S, D, causal):
     dev = device()
@@ -197,3 +197,27 @@ def test_varlen_from_fused_qkv(D):
     assert cga.device_status() == 0
     check_out(o_store.transpose(1, 2), o_ref, "bf16_pre", f"fused-qkv varlen D{D}")
     check_lse(lse, lse_ref, f"fused-qkv varlen D{D} lse")
+
+
+@pytest.mark.parametrize("D", [128, 64])
+def test_key_split_sampled(D):
+    """B1 Hq8 S6144: between one and two waves of two-tile blocks, where the planner splits the
+    late row blocks' key tiles into segments and a second kernel merges them. Rows sampled
+    (every 64th and the last 128 of each head: the split row blocks are the late ones)."""
+    dev = device()
+    B, Hq, Hkv, S = 1, 8, 2, 6144
+    q, k, v = workloads.prefill_inputs(B, Hq, Hkv, S, D, "bf16", 3.0, seed=9)
+    rows = sampled_rows(B, Hq, S)
+    o_ref, lse_ref = oracle.prefill(q, k, v, True, 1 / math.sqrt(D), rows=rows)
+    idx = torch.as_tensor(rows, device=dev)
+    for dt, kind in ((torch.float32, "bf16_pre"), (torch.bfloat16, "bf16")):
+        o, lse = _run(q.to(dev), k.to(dev), v.to(dev), True, dt)
+        check_out(o.reshape(-1, D)[idx], o_ref, kind, f"split S6144 D{D} {kind}")
+        check_lse(lse.reshape(-1)[idx], lse_ref, f"split S6144 D{D} lse")
+    # the merge kernel writes through the output's strides: a [B, S, Hq, D] buffer gives the
+    # same bits as the contiguous output
+    o1, l1 = _run(q.to(dev), k.to(dev), v.to(dev), True, torch.bfloat16)
+    o_store = torch.empty((B, S, Hq, D), dtype=torch.bfloat16, device=dev)
+    _, l2 = _run(_bshd(q, dev), _bshd(k, dev), _bshd(v, dev), True, torch.bfloat16,
+                 out=o_store.transpose(1, 2))
+    assert torch.equal(o1, o_store.transpose(1, 2)) and torch.equal(l1, l2)
