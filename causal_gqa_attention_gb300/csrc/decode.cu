@@ -259,6 +259,23 @@ __device__ __forceinline__ void load_bf16x8(const __nv_bfloat16 *src, float (&x)
     }
 }
 
+// q fragment as load_q, rotated by RoPE first (in fp32, never rounded).
+template <int D, int HG>
+__device__ __forceinline__ void load_q_rope(const __nv_bfloat16 *q, size_t row0, int gl,
+                                            float scale_log2, const float (&c)[8],
+                                            const float (&sv)[8], float2 (&qp)[HG][4])
+{
+#pragma unroll
+    for (int h = 0; h < HG; ++h) {
+        float x[8];
+        load_bf16x8(q + (row0 + h) * D + gl * 8, x);
+        rope_rotate8<D>(x, gl, c, sv);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            qp[h][e] = make_float2(x[2 * e] * scale_log2, x[2 * e + 1] * scale_log2);
+    }
+}
+
 // The new token's K/V for decode with RoPE (unrotated key, value, angle tables, and the cache
 // to store the rotated key and the value in). Unused (null) in plain decode.
 struct RopeIn {
@@ -472,148 +489,11 @@ __device__ __forceinline__ void cursor_advance(StreamCursor &c, int n, const int
     }
 }
 
-// ------------------------------------------------------------------ warp-level tensor-core steps
-// The stream kernel's stage update computes with the m16n8k16 warp MMA (bf16 in, fp32
-// accumulate). Scores are formed transposed, S^T = K Q^T (16 keys x 8 heads of one stream, the
-// heads of the stream sharing every K row), and the output as O^T = V^T P^T (16 dims x 8 heads),
-// so the key rows are the MMA's M side and the group's heads fill its N = 8 side; the contraction
-// is there anyway, and one MMA does the multiply-adds of about 180 scalar fused multiply-adds
-// plus their bf16 widening, which is what bounded the warp's issue rate.
-// Fragment layouts (lane = 4 * gid + tig): A (16 x 16): {row gid, cols 2tig, 2tig+1},
-// {row gid+8, same}, {row gid, cols +8}, {row gid+8, cols +8}; B (16 x 8): {rows 2tig, 2tig+1,
-// col gid}, {rows +8}; C (16 x 8): {row gid, cols 2tig, 2tig+1}, {row gid+8, same}.
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1)
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// Four 8x8 b16 matrices from shared memory; lane i gives the address of row i % 8 of matrix
-// i / 8. The .trans form hands each lane its elements of the transposed matrices.
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
-}
-
-// Transpose of an 8x8 b16 matrix held one row pair per lane (C layout -> B layout).
-__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x)
-{
-    uint32_t y;
-    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
-    return y;
-}
-
-// Compile-time plan of the stream kernel for head dim D (the N = 8 side holds up to 8 heads).
-template <int D>
-struct SPlan {
-    static constexpr int SK = D == 128 ? 16 : 32;  // keys per stage: 8 KB of K and V rows
-    static constexpr int MT = SK / 16;             // 16-key score tiles per stage
-    static constexpr int KS = D / 16;              // 16-dim steps of S^T = tiles of O^T
-    static constexpr int ROW = D * 2;              // bytes of one K or V row
-    // Rows are copied two at a time (512 or 256 bytes per bulk copy) into 16-byte-padded
-    // blocks, so the blocks of eight consecutive row pairs start in eight different bank quads.
-    // An MMA tile's row m is key 2 (m % 8) + m / 8 of its 16: each 8-row matrix that ldmatrix
-    // reads takes one row from each of eight blocks, free of bank conflicts.
-    static constexpr int RPC = 2;                  // rows per bulk copy (contiguous in smem)
-    static constexpr int BLK = RPC * ROW + 16;     // smem bytes per copied block, padded
-    static constexpr int VB = (SK / RPC) * BLK;    // V rows start here
-    static constexpr int STAGE = 2 * VB;           // K rows, then V rows
-    // smem offset of row r of the K (or V) part; r0 + r1 maps to the sum when r0 % RPC == 0
-    static __device__ __forceinline__ int rowoff(int r) { return (r / RPC) * BLK + (r % RPC) * ROW; }
-    static constexpr int RING = kWarps * kRing * STAGE;
-    static constexpr int BARS = kWarps * kRing * 8;
-    static constexpr int SMEM = RING + BARS;
-};
-
-// B fragments of Q^T for the MMA S^T = K Q^T: lane (gid, tig) holds head gid (zero past HG) at
-// dims 16kk + 2tig + {0, 1} and + {8, 9} of every 16-dim step kk.
-template <int D, int HG>
-__device__ __forceinline__ void load_q_frag(const __nv_bfloat16 *q, size_t row0, int lane,
-                                            uint32_t (&qf)[D / 16][2])
-{
-    const int gid = lane / 4, tig = lane % 4;
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-        if (gid < HG) {
-            const uint32_t *src =
-                reinterpret_cast<const uint32_t *>(q + (row0 + gid) * D + kk * 16 + tig * 2);
-            qf[kk][0] = src[0];
-            qf[kk][1] = src[4];
-        } else {
-            qf[kk][0] = qf[kk][1] = 0u;
-        }
-    }
-}
-
-// As load_q_frag, with q first rotated by RoPE (rotate-half, angles of row `prow` of the
-// tables) in fp32 and then split into bf16 high and low parts (q = hi + lo to about 2^-17), so
-// the scores keep the unrounded rotation. A lane's dims 16kk + {2tig, 2tig+1, 2tig+8, 2tig+9}
-// for kk < KS/2 pair with the same offsets in step kk + KS/2, so it rotates its own pairs.
-template <int D, int HG>
-__device__ __forceinline__ void load_q_frag_rope(const __nv_bfloat16 *q, size_t row0, int lane,
-                                                 const float *cs, const float *sn,
-                                                 uint32_t (&qh)[D / 16][2],
-                                                 uint32_t (&ql)[D / 16][2])
-{
-    constexpr int KS = D / 16, H = D / 2;
-    const int gid = lane / 4, tig = lane % 4;
-#pragma unroll
-    for (int kk = 0; kk < KS / 2; ++kk) {
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int d = kk * 16 + tig * 2 + half * 8;  // pairs d, d + 1 with d + H, d + H + 1
-            float x1[2] = {0.f, 0.f}, x2[2] = {0.f, 0.f}, c[2] = {1.f, 1.f}, s[2] = {0.f, 0.f};
-            if (gid < HG) {
-                const __nv_bfloat16 *r = q + (row0 + gid) * D;
-                const uint32_t w1 = *reinterpret_cast<const uint32_t *>(r + d);
-                const uint32_t w2 = *reinterpret_cast<const uint32_t *>(r + d + H);
-                x1[0] = bf16lo(w1); x1[1] = bf16hi(w1);
-                x2[0] = bf16lo(w2); x2[1] = bf16hi(w2);
-                const float2 cc = *reinterpret_cast<const float2 *>(cs + d);
-                const float2 ss = *reinterpret_cast<const float2 *>(sn + d);
-                c[0] = cc.x; c[1] = cc.y; s[0] = ss.x; s[1] = ss.y;
-            }
-            float y1[2], y2[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                y1[e] = x1[e] * c[e] - x2[e] * s[e];  // dim d + e
-                y2[e] = x1[e] * s[e] + x2[e] * c[e];  // dim d + H + e
-            }
-            const uint32_t a = pack_bf16x2(y1[0], y1[1]), b = pack_bf16x2(y2[0], y2[1]);
-            qh[kk][half] = a;
-            qh[kk + KS / 2][half] = b;
-            ql[kk][half] = pack_bf16x2(y1[0] - bf16lo(a), y1[1] - bf16hi(a));
-            ql[kk + KS / 2][half] = pack_bf16x2(y2[0] - bf16lo(b), y2[1] - bf16hi(b));
-        }
-    }
-}
-
 // ROPE: the step also applies RoPE to q and to the new key at position seqlens[b] - 1 and
 // stores the new key and value in the cache. The warp whose stage holds that row (the last key
 // of a stream) replaces the row in shared memory (it was loaded before the store) with the
 // rotated key, rounded to bf16 as the cache holds it, and the value; the stream of query-head
 // subgroup 0 of each kv head also writes them to the cache.
-//
-// Stage update (one stage of n <= SK keys of one stream, HG heads):
-//   S^T = K Q^T per 16-key tile (KS MMAs; twice with the RoPE q's low part), scaled to log2
-//   units, keys past n set to -inf; lane (gid, tig) holds tile rows gid, gid + 8 (keys 2gid,
-//   2gid + 1) of heads 2tig, 2tig + 1. The running max per head is rescaled lazily (only when a score exceeds it by 2^8).
-//   p = 2^(s - m) is split into bf16 high and low parts, each moved from the C layout to the
-//   B layout by an 8x8 transpose, and O^T += V^T P^T (KS MMAs per part per 16-key tile), V^T
-//   read with transposing ldmatrix from the row-major V rows.
 template <int D, int HG, bool ROPE>
 __global__ void __launch_bounds__(kWarps * 32)
     decode_stream_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ kc,
@@ -622,16 +502,15 @@ __global__ void __launch_bounds__(kWarps * 32)
                          int Hkv, int max_len, float scale_log2, unsigned *__restrict__ status,
                          RopeIn rope, long long wait_limit)
 {
-    using P = SPlan<D>;
-    constexpr int SK = P::SK, MT = P::MT, KS = P::KS, ROW = P::ROW, RPC = P::RPC, VB = P::VB;
-    constexpr int LPK = D / 8;  // lanes holding one row in 16-byte pieces (RoPE new key)
-    static_assert(HG <= 8, "the MMA's N side holds 8 heads");
+    using P = Plan<D, HG>;
+    constexpr int LPK = P::LPK, GPW = P::GPW, T = P::T, NV = P::NV, SK = P::SK;
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *ring = smem;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + P::RING);
+    float2 *pbuf = reinterpret_cast<float2 *>(smem + P::RING);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + P::RING + P::PBUF);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int gid = lane / 4, tig = lane % 4;
+    const int grp = lane / LPK, gl = lane % LPK;
     const int G = Hq / Hkv, SUB = G / HG, NGS = Hkv * SUB;
     const int W = blockIdx.x * kWarps + warp, NWT = gridDim.x * kWarps;
 
@@ -686,8 +565,7 @@ __global__ void __launch_bounds__(kWarps * 32)
         c0.sl = (int)(rel / c0.Lb);
         c0.off = (int)(rel % c0.Lb);
 
-        // ---- producer side: every lane tracks the cursor; the stage's rows are copied one
-        // row per bulk copy (lanes in parallel) into the padded layout
+        // ---- producer side (lane 0 issues; every lane tracks the cursor)
         StreamCursor pc = c0;
         int issued = 0;
         auto issue_next = [&]() {
@@ -697,29 +575,21 @@ __global__ void __launch_bounds__(kWarps * 32)
             const int n = (int)min((long long)SK, min(left_piece, left_slice));
             const int slot = issued % kRing;
             uint8_t *dst = ring + (warp * kRing + slot) * P::STAGE;
-            uint64_t *bar = &bars[warp * kRing + slot];
             if (n < SK) {
                 // V rows past the copy get p = 0, and 0 * NaN would not be 0: zero them (the
                 // ring is not cleared at start, and a slot keeps an earlier stage's rows)
-                for (int c = lane; c < (SK - n) * (ROW / 16); c += 32) {
-                    const int r = n + c / (ROW / 16);
-                    *reinterpret_cast<uint4 *>(dst + VB + P::rowoff(r) + (c % (ROW / 16)) * 16) =
-                        make_uint4(0, 0, 0, 0);
-                }
+                uint4 *vz = reinterpret_cast<uint4 *>(dst + (SK + n) * P::ROW);
+                for (int c = lane; c < (SK - n) * P::ROW / 16; c += 32) vz[c] = make_uint4(0, 0, 0, 0);
+                fence_proxy_async_smem();
+                __syncwarp();
             }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_expect_tx(bar, 2u * n * ROW);
-            __syncwarp();
-            const int g = pc.sl / SUB;
-            const size_t row = ((size_t)pc.b * Hkv + g) * (size_t)max_len + pc.off;
-            const int nb = (n + RPC - 1) / RPC;  // copied blocks of K (and of V)
-            for (int c = lane; c < 2 * nb; c += 32) {
-                const bool isv = c >= nb;
-                const int bi = isv ? c - nb : c;
-                const int rows = min(RPC, n - bi * RPC);
-                bulk_load(dst + (isv ? VB : 0) + bi * P::BLK, (isv ? vc : kc) + (row + bi * RPC) * D,
-                          rows * ROW, bar);
+            if (lane == 0) {
+                const int g = pc.sl / SUB;
+                const size_t row = ((size_t)pc.b * Hkv + g) * (size_t)max_len + pc.off;
+                uint64_t *bar = &bars[warp * kRing + slot];
+                mbar_arrive_expect_tx(bar, 2u * n * P::ROW);
+                bulk_load(dst, kc + row * D, n * P::ROW, bar);
+                bulk_load(dst + SK * P::ROW, vc + row * D, n * P::ROW, bar);
             }
             cursor_advance(pc, n, seqlens, B, max_len, NGS);
             ++issued;
@@ -727,19 +597,13 @@ __global__ void __launch_bounds__(kWarps * 32)
         for (int r = 0; r < kRing; ++r) issue_next();
 
         // ---- consumer side
-        const int mj = lane / 8, mr = lane % 8;
-        // ldmatrix row addresses (tile row m is key 2 (m % 8) + m / 8): K as A of S^T (matrix j:
-        // tile rows + 8 (j & 1), dims + 8 (j >> 1)), V as the transposed A of O^T (matrix j: tile
-        // rows + 8 (j >> 1), dims + 8 (j & 1))
-        const uint32_t offK = (uint32_t)(P::rowoff(2 * mr + (mj & 1)) + (mj >> 1) * 16);
-        const uint32_t offV = (uint32_t)(VB + P::rowoff(2 * mr + (mj >> 1)) + (mj & 1) * 16);
-        const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(ring);
         StreamCursor cc = c0;
-        uint32_t qf[KS][2];
-        uint32_t qlo[ROPE ? KS : 1][2];
-        float o[KS][4];
-        float m_ref[2], l_own[2];
+        float2 qp[HG][4];
+        float m_ref[HG];
+        float2 acc[HG][4];
+        float l_own[NV];
         uint4 new_k = make_uint4(0, 0, 0, 0), new_v = new_k;  // RoPE: the new row, packed bf16
+        float2 *pw = pbuf + (warp * GPW + grp) * T * HG;
         volatile int never = 0;
         int it = 0;
         bool ok = true;
@@ -749,18 +613,16 @@ __global__ void __launch_bounds__(kWarps * 32)
             const bool last = (cc.off + n == cc.Lb) || (cc.pos + n == r1);
             if (first) {
                 const int g = cc.sl / SUB, gs = cc.sl % SUB;
-                const size_t qrow = (size_t)cc.b * Hq + g * G + gs * HG;
                 if constexpr (ROPE) {
                     // angles of the newest token's position, for q and (when this slice ends
                     // the stream) for the new key, which is rotated and packed here so the
                     // stage that holds its row needs no global load
                     const size_t prow = (size_t)(cc.Lb - 1) * (D / 2);
-                    load_q_frag_rope<D, HG>(q, qrow, lane, rope.cos_t + prow, rope.sin_t + prow,
-                                            qf, qlo);
+                    float c[8], sv[8];
+                    rope_angles<D>(gl, rope.cos_t + prow, rope.sin_t + prow, c, sv);
+                    load_q_rope<D, HG>(q, (size_t)cc.b * Hq + g * G + gs * HG, gl, scale_log2,
+                                       c, sv, qp);
                     if (cc.pos + (cc.Lb - cc.off) <= r1) {
-                        const int gl = lane % LPK;
-                        float c[8], sv[8];
-                        rope_angles<D>(gl, rope.cos_t + prow, rope.sin_t + prow, c, sv);
                         const size_t src = ((size_t)cc.b * Hkv + g) * D + gl * 8;
                         float x[8];
                         load_bf16x8(rope.k_new + src, x);
@@ -770,25 +632,30 @@ __global__ void __launch_bounds__(kWarps * 32)
                         new_v = *reinterpret_cast<const uint4 *>(rope.v_new + src);
                     }
                 } else {
-                    load_q_frag<D, HG>(q, qrow, lane, qf);
+                    load_q<D, HG, __nv_bfloat16>(q, (size_t)cc.b * Hq + g * G + gs * HG, gl,
+                                                 scale_log2, qp);
                 }
-                m_ref[0] = m_ref[1] = -INFINITY;
-                l_own[0] = l_own[1] = 0.f;
 #pragma unroll
-                for (int k = 0; k < KS; ++k) o[k][0] = o[k][1] = o[k][2] = o[k][3] = 0.f;
+                for (int h = 0; h < HG; ++h) {
+                    m_ref[h] = -INFINITY;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[h][e] = make_float2(0.f, 0.f);
+                }
+#pragma unroll
+                for (int v = 0; v < NV; ++v) l_own[v] = 0.f;
             }
             const int slot = it % kRing;
             ok = __all_sync(0xffffffffu,
                             mbar_wait(&bars[warp * kRing + slot], (it / kRing) & 1, &never, wait_limit));
             if (!ok) break;
-            uint8_t *stg = ring + (warp * kRing + slot) * P::STAGE;
             if constexpr (ROPE) {
                 if (cc.off + n == cc.Lb) {  // the stage holds the newest key, as its row n - 1
-                    const int g = cc.sl / SUB, gl = lane % LPK;
+                    const int g = cc.sl / SUB;
                     const uint4 kw = new_k, vw = new_v;
-                    if (lane < LPK) {
-                        *reinterpret_cast<uint4 *>(stg + P::rowoff(n - 1) + gl * 16) = kw;
-                        *reinterpret_cast<uint4 *>(stg + VB + P::rowoff(n - 1) + gl * 16) = vw;
+                    if (grp == 0) {
+                        uint8_t *stg = ring + (warp * kRing + slot) * P::STAGE;
+                        *reinterpret_cast<uint4 *>(stg + (n - 1) * P::ROW + gl * 16) = kw;
+                        *reinterpret_cast<uint4 *>(stg + (SK + n - 1) * P::ROW + gl * 16) = vw;
                         if (cc.sl % SUB == 0) {
                             const size_t row =
                                 (((size_t)cc.b * Hkv + g) * max_len + (cc.Lb - 1)) * D + gl * 8;
@@ -799,101 +666,45 @@ __global__ void __launch_bounds__(kWarps * 32)
                     __syncwarp();
                 }
             }
-            const uint32_t sbase = ring_s + (uint32_t)((warp * kRing + slot) * P::STAGE);
-            // ---- scores S^T (keys x heads), log2 units, keys past n masked
-            float s[MT][4];
+            stage_update<D, HG>(ring + (warp * kRing + slot) * P::STAGE, n, grp, gl, qp, m_ref,
+                                acc, l_own, pw);
+            if (last) {
+                float lsum[HG];
+                group_sums<D, HG>(l_own, gl, lsum);
+                // combine the GPW groups of the warp (lanes gl, gl + LPK, ...)
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = 0.f;
+                for (int off = LPK; off < 32; off <<= 1) {
 #pragma unroll
-                for (int kk = 0; kk < KS; ++kk) {
-                    uint32_t a[4];
-                    ldsm_x4(a, sbase + offK + P::rowoff(mt * 16) + kk * 32);
-                    mma_bf16(s[mt], a, qf[kk][0], qf[kk][1]);
-                    if constexpr (ROPE) mma_bf16(s[mt], a, qlo[kk][0], qlo[kk][1]);
-                }
-            }
-            bool need = false;
+                    for (int h = 0; h < HG; ++h) {
+                        const float mo = __shfl_xor_sync(0xffffffffu, m_ref[h], off);
+                        const float mn = fmaxf(m_ref[h], mo);
+                        const float mu = (mn == -INFINITY) ? 0.f : mn;
+                        const float a = ex2(m_ref[h] - mu);
+                        lsum[h] *= a;
+                        lsum[h] += __shfl_xor_sync(0xffffffffu, lsum[h], off);
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int key = mt * 16 + 2 * gid + (e >= 2 ? 1 : 0);  // tile rows gid, gid + 8
-                    const float x = s[mt][e] * scale_log2;
-                    s[mt][e] = key < n ? x : -INFINITY;
-                    need |= s[mt][e] > m_ref[e & 1] + 8.0f;
-                }
-            if (__any_sync(0xffffffffu, need)) {
-                // exact max per head over the stage's keys (lanes of equal tig), then rescale
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    float bm = -INFINITY;
-#pragma unroll
-                    for (int mt = 0; mt < MT; ++mt) bm = fmaxf(bm, fmaxf(s[mt][h], s[mt][h + 2]));
-#pragma unroll
-                    for (int off = 4; off < 32; off <<= 1)
-                        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
-                    const float mn = fmaxf(m_ref[h], bm);
-                    if (mn > m_ref[h]) {
-                        const float alpha = ex2(m_ref[h] - mn);  // 0 when m_ref was -inf
-#pragma unroll
-                        for (int k = 0; k < KS; ++k) {
-                            o[k][h] *= alpha;
-                            o[k][h + 2] *= alpha;
+                        for (int e = 0; e < 4; ++e) {
+                            acc[h][e] = fmul2(acc[h][e], make_float2(a, a));
+                            acc[h][e].x += __shfl_xor_sync(0xffffffffu, acc[h][e].x, off);
+                            acc[h][e].y += __shfl_xor_sync(0xffffffffu, acc[h][e].y, off);
                         }
-                        l_own[h] *= alpha;
                         m_ref[h] = mn;
                     }
                 }
-            }
-            const float mu0 = m_ref[0] == -INFINITY ? 0.f : m_ref[0];
-            const float mu1 = m_ref[1] == -INFINITY ? 0.f : m_ref[1];
-            // ---- O^T += V^T P^T, P in bf16 high and low parts
+                if (grp == 0) {
+                    const size_t piece = (size_t)W + (size_t)cc.b * NGS + cc.sl;
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                const float p0 = ex2(s[mt][0] - mu0), p1 = ex2(s[mt][1] - mu1);
-                const float p2 = ex2(s[mt][2] - mu0), p3 = ex2(s[mt][3] - mu1);
-                l_own[0] += p0 + p2;
-                l_own[1] += p1 + p3;
-                const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
-                const uint32_t l01 = pack_bf16x2(p0 - bf16lo(h01), p1 - bf16hi(h01));
-                const uint32_t l23 = pack_bf16x2(p2 - bf16lo(h23), p3 - bf16hi(h23));
-                const uint32_t bh0 = movmatrix_t(h01), bh1 = movmatrix_t(h23);
-                const uint32_t bl0 = movmatrix_t(l01), bl1 = movmatrix_t(l23);
-#pragma unroll
-                for (int k = 0; k < KS; ++k) {
-                    uint32_t a[4];
-                    ldsm_x4_t(a, sbase + offV + P::rowoff(mt * 16) + k * 32);
-                    mma_bf16(o[k], a, bh0, bh1);
-                    mma_bf16(o[k], a, bl0, bl1);
-                }
-            }
-            if (last) {
-                // sums per head over the 8 key lanes, then the piece's partial state
-                float lsum[2];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    float x = l_own[h];
-#pragma unroll
-                    for (int off = 4; off < 32; off <<= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-                    lsum[h] = x;
-                }
-                const size_t piece = (size_t)W + (size_t)cc.b * NGS + cc.sl;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int head = 2 * tig + h;
-                    if (head < HG) {
-                        float *dst = ws_o + (piece * HG + head) * D + gid;
-#pragma unroll
-                        for (int k = 0; k < KS; ++k) {
-                            dst[k * 16] = o[k][h];
-                            dst[k * 16 + 8] = o[k][h + 2];
-                        }
-                        if (gid == 0) ws_ml[piece * HG + head] = make_float2(m_ref[h], lsum[h]);
+                    for (int h = 0; h < HG; ++h) {
+                        float4 *dst = reinterpret_cast<float4 *>(ws_o + (piece * HG + h) * D + gl * 8);
+                        dst[0] = make_float4(acc[h][0].x, acc[h][0].y, acc[h][1].x, acc[h][1].y);
+                        dst[1] = make_float4(acc[h][2].x, acc[h][2].y, acc[h][3].x, acc[h][3].y);
+                        if (gl == 0) ws_ml[piece * HG + h] = make_float2(m_ref[h], lsum[h]);
                     }
                 }
             }
-            issue_next();  // its proxy fence orders this stage's reads before the slot's refill
+            if (lane == 0) fence_proxy_async_smem();
+            __syncwarp();
+            issue_next();
             cursor_advance(cc, n, seqlens, B, max_len, NGS);
             ++it;
         }
@@ -1172,7 +983,7 @@ int largest_group(int G)
 template <int D, int HG, bool ROPE>
 cudaError_t launch_stream_t(const DecodeArgs &a, bool out_f32, cudaStream_t st)
 {
-    using P = SPlan<D>;
+    using P = Plan<D, HG>;
     constexpr auto kern = decode_stream_kernel<D, HG, ROPE>;
     static bool attr_set[64] = {};
     static int blocks_cached[64] = {};
@@ -1182,13 +993,13 @@ cudaError_t launch_stream_t(const DecodeArgs &a, bool out_f32, cudaStream_t st)
     int blocks = dev < 64 ? blocks_cached[dev] : 0;
     if (dev >= 64 || !attr_set[dev]) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 P::SMEM);
+                                 P::RING + P::PBUF + P::BARS);
         if (e != cudaSuccess) return e;
         int sms = 0, occ = 0;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kWarps * 32,
-                                                          P::SMEM);
+                                                          P::RING + P::PBUF + P::BARS);
         if (e != cudaSuccess) return e;
         blocks = sms * (occ > 0 ? occ : 1);
         if (blocks * kWarps > kStreamMaxWarps) blocks = kStreamMaxWarps / kWarps;
@@ -1213,7 +1024,7 @@ cudaError_t launch_stream_t(const DecodeArgs &a, bool out_f32, cudaStream_t st)
         rope.kc = static_cast<__nv_bfloat16 *>(const_cast<void *>(a.kc));
         rope.vc = static_cast<__nv_bfloat16 *>(const_cast<void *>(a.vc));
     }
-    e = launch_pdl(kern, dim3(blocks), dim3(kWarps * 32), P::SMEM, st,
+    e = launch_pdl(kern, dim3(blocks), dim3(kWarps * 32), P::RING + P::PBUF + P::BARS, st,
                    static_cast<const __nv_bfloat16 *>(a.q), static_cast<const __nv_bfloat16 *>(a.kc),
                    static_cast<const __nv_bfloat16 *>(a.vc), a.seqlens, ws_o, ws_ml, a.B, a.Hq,
                    a.Hkv, a.max_len, a.scale_log2, a.status, rope, wait_limit_cycles());
