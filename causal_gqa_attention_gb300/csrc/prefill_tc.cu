@@ -365,6 +365,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_4d(smem + kOffQ + t * kTile + x * kBox, &tq, &bar[B_Q], x * 64,
                                 q0 + t * BM, h, b);
             int issued_k[KST] = {}, issued_v[VST] = {};
+            auto load_k = [&](int jj) {
+                const int sk = jj % KST, uk = jj / KST;
+                mbar_arrive_expect_tx(&bar[B_KFULL + sk], kTile);
+                for (int x = 0; x < G::NBOX; ++x)
+                    tma_load_4d(smem + kOffK + sk * kTile + x * kBox, &tk, &bar[B_KFULL + sk],
+                                x * 64, (jb + jj) * BN, g, b);
+                issued_k[sk] = uk + 1;
+            };
+            // the first KST key tiles need no stage to be freed: load them before waiting for
+            // the V conversion, so the first scores of both tiles can run meanwhile
+            for (int jj = 0; jj < KST && jj < nJ; ++jj) load_k(jj);
             for (int jj = 0; jj < nJ; ++jj) {
                 const int j = jb + jj;
                 // K_jj and V_jj reuse the stages of K_jj-2 and V_jj-3, both last read by the
@@ -372,12 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (jj >= 2 &&
                     !mbar_wait(&bar[B_STEP + ((jj - 2) & 1)], ((jj - 2) >> 1) & 1, abort_flag, wait_limit))
                     break;
-                const int sk = jj % KST, uk = jj / KST;
-                mbar_arrive_expect_tx(&bar[B_KFULL + sk], kTile);
-                for (int x = 0; x < G::NBOX; ++x)
-                    tma_load_4d(smem + kOffK + sk * kTile + x * kBox, &tk, &bar[B_KFULL + sk],
-                                x * 64, j * BN, g, b);
-                issued_k[sk] = uk + 1;
+                if (jj >= KST) load_k(jj);
                 // the fp16 copy of V comes from the conversion kernel just before this one,
                 // which lets this grid start early (programmatic dependent launch): everything
                 // up to here overlaps its tail
