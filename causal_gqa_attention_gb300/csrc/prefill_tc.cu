@@ -395,6 +395,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 x * 64, j * BN, g, b);
                 issued_v[sv] = uv + 1;
             }
+            // Every load of this block is issued: warm L2 with the Q tiles of the block that
+            // will most likely run on this SM next (one block per SM at a time, launched in
+            // order, so about one SM count further on), whose set-up otherwise waits on DRAM.
+            if (!SPLIT) {
+                uint32_t nsm;
+                asm("mov.u32 %0, %%nsmid;" : "=r"(nsm));
+                const int nb = (int)blockIdx.x + (int)nsm;
+                if (nb < (int)gridDim.x) {
+                    const int nrb = n_rb - 1 - nb / (Hq * B), nhb = nb % (Hq * B);
+                    const int nq0 = nrb * RB;
+                    for (int t = 0; t < (PAIR ? 1 : 2) && nq0 + t * BM < S; ++t)
+                        for (int x = 0; x < G::NBOX; ++x)
+                            tma_prefetch_4d(&tq, x * 64, nq0 + t * BM, nhb % Hq, nhb / Hq);
+                }
+            }
             if (*abort_flag) {
                 // let every copy this block started land before the block exits
                 mbar_wait_drain(&bar[B_Q], 0);
