@@ -627,13 +627,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_ref = m_new;
             }
             const bool active = hi[t] >= first_j[t];  // warp-uniform
+            // V was used as v * 2^-e: O comes out multiplied by 2^e. The exponent is read
+            // before the wait for the last P V, so its latency overlaps that wait.
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            const int vexp_e = vexp[b * Hkv + g];
             if (ok && active)
                 ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_OFULL + t], 0, abort_flag, wait_limit));
             // a row block whose keys fit in one segment writes its final result directly
             const bool direct = SPLIT && rb_segments(rb, S, causal, J, RB) == 1;
-            // V was used as v * 2^-e: O comes out multiplied by 2^e
-            asm volatile("griddepcontrol.wait;" ::: "memory");
-            const float osc = exp2i(vexp[b * Hkv + g]);
+            const float osc = exp2i(vexp_e);
             if constexpr (PAIR) {
                 // Both warpgroups hold (m, l, O) of the same rows over different key tiles. Each
                 // posts its (m, l) in the second Q buffer (never loaded in pair mode), then
