@@ -17,7 +17,8 @@ from __future__ import annotations
 import math
 
 from . import _lib
-from ._lib import (ATTN_BF16, ATTN_DEV_SEQLEN_CLAMPED, ATTN_DEV_WAIT_TIMEOUT, ATTN_ERR_ALIGN,
+from ._lib import (ATTN_BF16, ATTN_DEV_INDEX_CHECK, ATTN_DEV_SEQLEN_CLAMPED, ATTN_DEV_WAIT_TIMEOUT,
+                   ATTN_ERR_ALIGN,
                    ATTN_ERR_CUDA, ATTN_ERR_INVALID, ATTN_ERR_TIMEOUT, ATTN_ERR_UNSUPPORTED,
                    ATTN_ERR_WORKSPACE, ATTN_F32, ATTN_OK, AttnError)
 
@@ -28,10 +29,12 @@ __all__ = [
     "attn_decode", "attn_decode_ex",
     "attn_decode_noalloc", "chunk", "attn_decode_rope", "decode_rope",
     "attn_decode_workspace_bytes", "attn_decode_chunk_len", "attn_reserve_workspace",
-    "attn_device_status", "attn_debug_set_wait_limit", "attn_status_string", "attn_version", "prefill", "decode",
+    "attn_device_status", "attn_debug_set_wait_limit", "attn_status_string", "attn_version",
+    "attn_debug_build", "prefill", "decode",
     "device_status", "AttnError", "ATTN_OK", "ATTN_ERR_INVALID", "ATTN_ERR_UNSUPPORTED",
     "ATTN_ERR_ALIGN", "ATTN_ERR_WORKSPACE", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "ATTN_F32",
-    "ATTN_BF16", "ATTN_DEV_SEQLEN_CLAMPED", "ATTN_DEV_WAIT_TIMEOUT", "load_library",
+    "ATTN_BF16", "ATTN_DEV_SEQLEN_CLAMPED", "ATTN_DEV_WAIT_TIMEOUT", "ATTN_DEV_INDEX_CHECK",
+    "load_library",
 ]
 
 
@@ -151,6 +154,10 @@ def attn_status_string(code):
 
 def attn_version():
     return _lib.load().attn_version()
+
+
+def attn_debug_build():
+    return _lib.load().attn_debug_build()
 
 
 # ------------------------------------------------------------------ torch tensor front end

@@ -10,6 +10,8 @@ import threading
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libgqa_attn.so")
+# the build with device-side index checks, used when GQA_ATTN_DEBUG=1 (built on first use)
+DEBUG_LIB_PATH = os.path.join(_HERE, "_build", "libgqa_attn_debug.so")
 
 ATTN_OK = 0
 ATTN_ERR_INVALID = 1
@@ -22,6 +24,7 @@ ATTN_F32 = 0
 ATTN_BF16 = 1
 ATTN_DEV_SEQLEN_CLAMPED = 0x1
 ATTN_DEV_WAIT_TIMEOUT = 0x2
+ATTN_DEV_INDEX_CHECK = 0x4
 ATTN_DECODE_NOALLOC_SCRATCH_BYTES = 4 * 1024 * 1024
 
 _vp = ctypes.c_void_p
@@ -59,6 +62,7 @@ SIGNATURES = {
     "attn_device_status": (_i, [_vp, ctypes.POINTER(ctypes.c_uint)]),
     "attn_status_string": (ctypes.c_char_p, [_i]),
     "attn_version": (_i, []),
+    "attn_debug_build": (_i, []),
 }
 
 _lock = threading.Lock()
@@ -71,12 +75,21 @@ class AttnError(RuntimeError):
         super().__init__(f"{fn} failed: {status_string(code)} (code {code})")
 
 
+def debug_requested() -> bool:
+    return os.environ.get("GQA_ATTN_DEBUG", "") == "1"
+
+
 def load(path: str | None = None) -> ctypes.CDLL:
-    """The loaded CUDA library. Raises if it has not been built (run ``build()``)."""
+    """The loaded CUDA library. Raises if it has not been built (run ``build()``). With
+    GQA_ATTN_DEBUG=1 in the environment this is the debug build (compiled on first use)."""
     global _lib
     with _lock:
         if _lib is None or path is not None:
             p = path or LIB_PATH
+            if path is None and debug_requested():
+                from causal_gqa_attention_gb300 import build as _build
+
+                p = _build.build(debug=True)
             if not os.path.exists(p):
                 raise RuntimeError(
                     f"CUDA library {p} is missing; build it with "

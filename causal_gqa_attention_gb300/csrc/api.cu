@@ -333,6 +333,15 @@ extern "C" {
 
 int attn_version(void) { return 100; }
 
+int attn_debug_build(void)
+{
+#ifdef GQA_ATTN_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
+}
+
 const char *attn_status_string(int s)
 {
     switch (s) {

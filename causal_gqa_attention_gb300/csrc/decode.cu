@@ -341,6 +341,10 @@ __global__ void __launch_bounds__(kWarps * 32)
         const uint32_t n = (uint32_t)min(SK, end - k0);
         uint8_t *dst = ring + (warp * kRing + slot) * P::STAGE;
         uint64_t *bar = &bars[warp * kRing + slot];
+        if (!dbg_ok(n >= 1 && k0 + (int)n <= max_len, status)) {
+            mbar_arrive(bar);  // nothing copied: the stage completes empty
+            return;
+        }
         mbar_arrive_expect_tx(bar, 2u * n * P::ROW);
         bulk_load(dst, kb + (size_t)k0 * D, n * P::ROW, bar);
         bulk_load(dst + SK * P::ROW, vb + (size_t)k0 * D, n * P::ROW, bar);
@@ -425,6 +429,7 @@ __global__ void __launch_bounds__(kWarps * 32)
             a = fmaf(w, row[d], a);
         }
         const size_t orow = ((size_t)b * Hq + h0 + h) * nsplit + split;
+        if (!dbg_ok(orow < (size_t)gridDim.z * Hq * nsplit, status)) continue;
         ws_o[orow * D + d] = a;
         if (d == 0) ws_ml[orow] = make_float2(M, Ls);
     }
@@ -587,9 +592,13 @@ __global__ void __launch_bounds__(kWarps * 32)
                 const int g = pc.sl / SUB;
                 const size_t row = ((size_t)pc.b * Hkv + g) * (size_t)max_len + pc.off;
                 uint64_t *bar = &bars[warp * kRing + slot];
-                mbar_arrive_expect_tx(bar, 2u * n * P::ROW);
-                bulk_load(dst, kc + row * D, n * P::ROW, bar);
-                bulk_load(dst + SK * P::ROW, vc + row * D, n * P::ROW, bar);
+                if (dbg_ok(pc.b < B && g < Hkv && n >= 1 && pc.off + n <= max_len, status)) {
+                    mbar_arrive_expect_tx(bar, 2u * n * P::ROW);
+                    bulk_load(dst, kc + row * D, n * P::ROW, bar);
+                    bulk_load(dst + SK * P::ROW, vc + row * D, n * P::ROW, bar);
+                } else {
+                    mbar_arrive(bar);  // nothing copied: the stage completes empty
+                }
             }
             cursor_advance(pc, n, seqlens, B, max_len, NGS);
             ++issued;
@@ -691,7 +700,10 @@ __global__ void __launch_bounds__(kWarps * 32)
                         m_ref[h] = mn;
                     }
                 }
-                if (grp == 0) {
+                // piece (warp W, stream s) is row W + s of at most NWT + B * NGS
+                if (grp == 0 &&
+                    dbg_ok((size_t)W + (size_t)cc.b * NGS + cc.sl < (size_t)NWT + (size_t)B * NGS,
+                           status)) {
                     const size_t piece = (size_t)W + (size_t)cc.b * NGS + cc.sl;
 #pragma unroll
                     for (int h = 0; h < HG; ++h) {
@@ -729,7 +741,7 @@ __global__ void __launch_bounds__(MW * 32)
     decode_stream_merge_kernel(const float *__restrict__ ws_o, const float2 *__restrict__ ws_ml,
                                const int *__restrict__ seqlens, void *__restrict__ o,
                                float *__restrict__ lse, int B, int Hq, int Hkv, int max_len,
-                               int nwt)
+                               int nwt, unsigned *__restrict__ status)
 {
     constexpr int DL = D / 32;
     constexpr int PW = 8;  // pieces per warp per round
@@ -747,8 +759,10 @@ __global__ void __launch_bounds__(MW * 32)
     const int Lb = clamp_len(seqlens[b], max_len);
     const long long start = base + (long long)sl * Lb;
     const int wf = (int)(start / KP);
-    const int n = Lb > 0 ? (int)((start + Lb - 1) / KP) - wf + 1 : 0;
+    int n = Lb > 0 ? (int)((start + Lb - 1) / KP) - wf + 1 : 0;
     const size_t row0 = ((size_t)wf + (size_t)b * NGS + sl) * HG + hl;  // piece j: row0 + j*HG
+    if (!dbg_ok(n == 0 || row0 + (size_t)(n - 1) * HG < (size_t)nwt * HG + (size_t)B * Hq, status))
+        n = 0;
     // Everything above reads only seqlens, which the stream kernel does not write: this grid is
     // launched once every stream block has passed its own dependency wait, so whatever wrote
     // seqlens before the stream kernel has finished. Only the partials need the wait, which
@@ -1045,7 +1059,7 @@ cudaError_t launch_stream_t(const DecodeArgs &a, bool out_f32, cudaStream_t st)
                          : (many ? decode_stream_merge_kernel<false, D, HG, 4>
                                  : decode_stream_merge_kernel<false, D, HG, 16>);
     return cudaLaunchKernelEx(&cfg, merge, (const float *)ws_o, (const float2 *)ws_ml, a.seqlens,
-                              a.o, a.lse, a.B, a.Hq, a.Hkv, a.max_len, nwt);
+                              a.o, a.lse, a.B, a.Hq, a.Hkv, a.max_len, nwt, a.status);
 }
 
 template <int D, bool ROPE>

@@ -281,6 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = hb % Hq, b = hb / Hq;
     const int g = h / (Hq / Hkv);
     const int q0 = rb * RB;
+    // the block's work item must lie inside the problem (nothing is set up yet: leave at once)
+    if (!dbg_ok(rb >= 0 && rb < n_rb && b < B && g < Hkv, status)) return;
     // Keys: L of them. Plain prefill: L = S. Chunk against a cache (kv_lens given): the S
     // queries are the last S of the L_b cached tokens, so query row i sits at key position
     // i + off, off = L_b - S.

@@ -9,6 +9,23 @@
 
 namespace gqa {
 
+// ---------------------------------------------------------------------------- debug checks
+
+// Index checks of the debug build (compiled with GQA_ATTN_DEBUG): a failed check sets bit
+// ATTN_DEV_INDEX_CHECK (0x4) of the device status word and the caller skips the access it
+// guards; nothing traps. In the regular build the check is compiled out (always true).
+__device__ __forceinline__ bool dbg_ok(bool cond, unsigned *status)
+{
+#ifdef GQA_ATTN_DEBUG
+    if (!cond) atomicOr(status, 0x4u);
+    return cond;
+#else
+    (void)status;
+    (void)cond;
+    return true;
+#endif
+}
+
 // ---------------------------------------------------------------------------- addresses
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)

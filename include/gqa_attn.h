@@ -62,6 +62,8 @@ typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype;
 /* Bits of the device status word (attn_device_status). */
 #define ATTN_DEV_SEQLEN_CLAMPED 0x1u /* decode: a seqlens[b] was < 0 or > max_len; clamped   */
 #define ATTN_DEV_WAIT_TIMEOUT 0x2u   /* a pipeline wait ran out; the block stopped          */
+#define ATTN_DEV_INDEX_CHECK 0x4u    /* debug build only: an index check in a kernel failed
+                                        and the access it guards was skipped               */
 
 /*
  * attn_prefill -- causal or non-causal prefill, bf16 in, bf16 out.
@@ -343,6 +345,17 @@ const char *attn_status_string(int status);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 int attn_version(void);
+
+/*
+ * attn_debug_build -- 1 in the debug build of this library, 0 otherwise. The pages give no
+ * debug build; it serves the checking of this implementation. The debug build (built on
+ * demand and loaded by the Python binding when GQA_ATTN_DEBUG=1) compiles in device-side
+ * checks of the kernels' index arithmetic: where a cache row range, a partial-result row or a
+ * block's work item would fall outside its buffer, the kernel sets ATTN_DEV_INDEX_CHECK in
+ * the status word and skips that access instead of trapping. Same entry points, same results;
+ * the checks cost a little speed.
+ */
+int attn_debug_build(void);
 
 #ifdef __cplusplus
 }

@@ -18,3 +18,16 @@ def oracle_lib():
     import oracle
 
     return oracle.load()
+
+
+@pytest.fixture(autouse=True)
+def _debug_build_index_checks(request):
+    """Under GQA_ATTN_DEBUG=1 (the debug build of the library, with device-side index checks),
+    every GPU test must end with no failed index check in the device status word."""
+    yield
+    if os.environ.get("GQA_ATTN_DEBUG", "") != "1" or request.node.get_closest_marker("gpu") is None:
+        return
+    import causal_gqa_attention_gb300 as cga
+
+    status = cga.device_status()
+    assert not status & cga.ATTN_DEV_INDEX_CHECK, f"index check failed (status {status:#x})"

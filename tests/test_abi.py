@@ -46,6 +46,18 @@ def test_library_exports_every_declared_symbol(lib):
         assert callable(getattr(cga, n)), f"binding lacks {n}"
 
 
+def test_debug_build_exports_the_same_symbols(lib):
+    """The debug build (device-side index checks) is the same library with the checks compiled
+    in: it builds without a GPU, exports every declared symbol and says it is the debug build."""
+    from causal_gqa_attention_gb300 import _lib, build
+
+    dbg = _lib.load(build.build(debug=True))
+    for n in _declared_functions():
+        assert hasattr(dbg, n), f"debug build lacks {n}"
+    assert dbg.attn_debug_build() == 1
+    assert lib.attn_debug_build() == 0
+
+
 def test_status_strings_and_version(lib):
     assert lib.attn_version() >= 100
     assert lib.attn_status_string(0) == b"ok"
