@@ -326,6 +326,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         hi[1] = min(je - 1, last_j[1]);
     }
 
+    if (!SPLIT && n_j == 0) {
+        // No row of the block sees a key (padding rows of a padded batch, an empty sequence):
+        // O = 0 and LSE = -inf, written without setting up barriers, TMEM or the roles.
+        for (int idx = threadIdx.x; idx < RB * (HD / 8); idx += kThreads) {
+            const int i = q0 + idx / (HD / 8), c = idx % (HD / 8);
+            if (i >= S) continue;
+            const long long e = b * o_sb + h * o_sh + (long long)i * o_ss + c * 8;
+            if (OUT_F32) {
+                float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(out) + e);
+                dst[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+                dst[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            } else {
+                *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(out) + e) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        if (lse != nullptr)
+            for (int r = threadIdx.x; r < RB; r += kThreads)
+                if (q0 + r < S) lse[((size_t)b * Hq + h) * S + q0 + r] = -INFINITY;
+        return;
+    }
+
     if (threadIdx.x == 0) {
         mbar_init(&bar[B_Q], 1);
         for (int s = 0; s < KST; ++s) mbar_init(&bar[B_KFULL + s], 1);
