@@ -46,6 +46,35 @@ def test_prefill_bf16_d64(B, Hq, Hkv, S, causal, q_mult):
     assert torch.equal(lse16, lse)
 
 
+# Head dim 64 on grids several waves deep: many heads (a group of 10 query heads per kv head),
+# short ragged sequences, a peaky softmax, and a longer batch checked on sampled rows.
+D64_MANY_HEADS = [
+    # B, Hq, Hkv, S, causal, q_mult
+    (4, 40, 8, 600, True, 1.0),
+    (4, 40, 8, 600, False, 1.0),
+    (2, 56, 8, 1100, True, 3.0),
+    (1, 160, 16, 1024, True, 1.0),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,causal,q_mult", D64_MANY_HEADS)
+def test_prefill_bf16_d64_many_heads(B, Hq, Hkv, S, causal, q_mult):
+    test_prefill_bf16_d64(B, Hq, Hkv, S, causal, q_mult)
+
+
+def test_prefill_bf16_d64_batch4_sampled():
+    dev = device()
+    B, Hq, Hkv, S = 4, 8, 2, 8192
+    q, k, v = workloads.prefill_inputs(B, Hq, Hkv, S, 64, "bf16", seed=9)
+    rows = sampled_rows(B, Hq, S)
+    o_ref, lse_ref = oracle.prefill(q, k, v, True, 1 / math.sqrt(64), rows=rows)
+    idx = torch.as_tensor(rows, device=dev)
+    for dt, kind in ((torch.float32, "bf16_pre"), (torch.bfloat16, "bf16")):
+        o, lse = _run(q.to(dev), k.to(dev), v.to(dev), True, dt)
+        check_out(o.reshape(-1, 64)[idx], o_ref, kind, f"d64 B4 S8192 {dt}")
+        check_lse(lse.reshape(-1)[idx], lse_ref, "d64 B4 S8192 lse")
+
+
 def test_prefill_bf16_d64_long_sampled():
     dev = device()
     B, Hq, Hkv, S = 2, 8, 2, 8192
@@ -98,6 +127,7 @@ def _bshd(t, dev):
 @pytest.mark.parametrize("B,Hq,Hkv,S,D,causal", [
     (2, 8, 2, 300, 128, True), (1, 4, 4, 1000, 128, False), (2, 8, 2, 700, 64, True),
     (1, 8, 2, 2048, 128, True),   # pair-mode blocks write through the strides
+    (4, 40, 8, 600, 64, True),    # head dim 64, many heads
 ])
 def test_prefill_bshd_layout(B, Hq, Hkv, S, D, causal):
     dev = device()
@@ -115,6 +145,7 @@ def test_prefill_bshd_layout(B, Hq, Hkv, S, D, causal):
 
 @pytest.mark.parametrize("B,Hq,Hkv,S,D,causal", [
     (2, 8, 2, 513, 128, True), (1, 16, 2, 256, 64, False), (3, 6, 2, 129, 128, True),
+    (2, 80, 8, 1024, 64, True),   # head dim 64, many heads
 ])
 def test_prefill_fused_qkv(B, Hq, Hkv, S, D, causal):
     """q, k, v as head slices of one [B, S, Hq + 2 Hkv, D] projection output; O written into a
@@ -135,10 +166,11 @@ def test_prefill_fused_qkv(B, Hq, Hkv, S, D, causal):
     assert torch.equal(qkv, before), "inputs were modified"
 
 
-def test_strided_equals_contiguous_bitwise():
+@pytest.mark.parametrize("B,Hq,Hkv,S,D", [(2, 8, 2, 1000, 128), (4, 40, 8, 600, 64)])
+def test_strided_equals_contiguous_bitwise(B, Hq, Hkv, S, D):
     """The same values through the strided entry and the contiguous one give identical bits."""
     dev = device()
-    q, k, v = workloads.prefill_inputs(2, 8, 2, 1000, 128, "bf16", seed=8)
+    q, k, v = workloads.prefill_inputs(B, Hq, Hkv, S, D, "bf16", seed=8)
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     o1, l1 = _run(qd, kd, vd, True, torch.bfloat16)
     o2, l2 = _run(_bshd(q, dev), _bshd(k, dev), _bshd(v, dev), True, torch.bfloat16)

@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 def _calls(cga, dev):
     """(name, fn) pairs covering the kernels with pipeline waits: prefill split + fp16 copy,
     unsplit prefill with V converted on chip (a workspace that holds only the V scale area),
-    the stream decode and the chunked decode (above 1024 sequences). The decode caches are
+    the stream decode, the chunked decode (above 1024 sequences) and a head-dim-64 prefill. The decode caches are
     large (1.1 GB each call) so that their pipelines wait on device memory, not on L2."""
     q, k, v = [t.to(dev) for t in workloads.prefill_inputs(1, 8, 2, 2048, 128, "bf16", seed=51)]
     small_ws = torch.empty(4096, dtype=torch.uint8, device=dev)
@@ -29,6 +29,9 @@ def _calls(cga, dev):
                          workloads.decode_inputs(32, 8, 2, 128, 32768, "full", seed=52)]
     bq, bkc, bvc, bsl = [t.to(dev) for t in
                          workloads.decode_inputs(1100, 2, 1, 128, 2048, "full", seed=53)]
+    # head dim 64, many heads (a grid several waves deep)
+    q4, k4, v4 = [t.to(dev) for t in workloads.prefill_inputs(2, 80, 8, 1024, 64, "bf16",
+                                                              seed=54)]
     return [
         ("prefill split", lambda: cga.prefill(q, k, v, causal=True, out_dtype=torch.float32,
                                               return_lse=True)),
@@ -38,13 +41,16 @@ def _calls(cga, dev):
                                       return_lse=True)),
         ("decode chunked", lambda: cga.decode(bq, bkc, bvc, bsl, out_dtype=torch.float32,
                                               return_lse=True)),
-    ], (q, k, v), (dq, dkc, dvc, dsl), (bq, bkc, bvc, bsl)
+        ("prefill d64", lambda: cga.prefill(q4, k4, v4, causal=True,
+                                                       out_dtype=torch.float32,
+                                                       return_lse=True)),
+    ], (q, k, v), (dq, dkc, dvc, dsl), (bq, bkc, bvc, bsl), (q4, k4, v4)
 
 
 def test_wait_timeout_is_reported_and_the_next_call_is_correct():
     cga = library()
     dev = device()
-    calls, pre, dec, big = _calls(cga, dev)
+    calls, pre, dec, big, pre4 = _calls(cga, dev)
     for _, fn in calls:  # first use: scratch sized, kernels loaded, with the normal bound
         fn()
     torch.cuda.synchronize()
@@ -79,3 +85,6 @@ def test_wait_timeout_is_reported_and_the_next_call_is_correct():
     ob_ref, lseb_ref = oracle.decode(*[t.cpu() for t in big], 1 / math.sqrt(128))
     check_out(results[3][0], ob_ref, "bf16_pre", "chunked decode after the timeouts")
     check_lse(results[3][1], lseb_ref, "chunked decode lse after the timeouts")
+    o4_ref, lse4_ref = oracle.prefill(*[t.cpu() for t in pre4], True, 1 / math.sqrt(64))
+    check_out(results[4][0], o4_ref, "bf16_pre", "d64 prefill after the timeouts")
+    check_lse(results[4][1], lse4_ref, "d64 prefill lse after the timeouts")
