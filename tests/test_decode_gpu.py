@@ -59,6 +59,11 @@ def test_decode_batched_other_seeds(seed):
     (3, 8, 2, 64, 513, [513, 64, 2]),        # D = 64
     (1, 8, 1, 128, 40000, [40000]),          # long context, one sequence over every warp
     (40, 8, 2, 128, 300, None),              # many short sequences per warp slice
+    (2, 4, 2, 128, 300, [300, 17]),          # G = 2: two heads per stream
+    (2, 12, 2, 64, 400, [400, 255]),         # G = 6: two heads per stream, three streams
+    (2, 32, 2, 128, 600, [600, 37]),         # G = 16: eight heads per stream, two streams
+    (2, 24, 2, 128, 500, [499, 250]),        # G = 12: four heads per stream, three streams
+    (2, 10, 2, 128, 300, [300, 1]),          # G = 5: one head per stream, five streams
 ])
 def test_decode_shapes(B, Hq, Hkv, D, max_len, lens):
     if lens is None:  # lengths 0..max_len, including empty sequences
@@ -115,11 +120,12 @@ def test_decode_seqlen_above_max_len_is_clamped_and_flagged():
     check_out(o, o_ref, "bf16_pre", "clamped length")
 
 
-def test_decode_large_batch_chunked_path():
-    """Batches above 1024 use the chunked split kernel."""
+@pytest.mark.parametrize("Hq,Hkv,D", [(8, 2, 128), (32, 2, 64), (3, 1, 128)])
+def test_decode_large_batch_chunked_path(Hq, Hkv, D):
+    """Batches above 1024 use the chunked split kernel (groups of 4, 16 and 3 query heads)."""
     B = 1100
     lens = torch.randint(1, 97, (B,), generator=torch.Generator().manual_seed(6))
     lens[::13] = 0
-    q, kc, vc, sl = workloads.decode_inputs(B, 8, 2, 128, 96, "explicit", seed=2,
+    q, kc, vc, sl = workloads.decode_inputs(B, Hq, Hkv, D, 96, "explicit", seed=2,
                                             seqlens=lens.tolist())
-    _check(q, kc, vc, sl, "decode B1100")
+    _check(q, kc, vc, sl, f"decode B1100 Hq{Hq} Hkv{Hkv} D{D}")
