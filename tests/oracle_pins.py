@@ -23,7 +23,8 @@ def _close(a, b, tol, what):
     a, b = np.asarray(a, dtype=np.float64), np.asarray(b, dtype=np.float64)
     assert a.shape == b.shape, (what, a.shape, b.shape)
     both_inf = np.isinf(a) & np.isinf(b) & (np.sign(a) == np.sign(b))
-    err = np.where(both_inf, 0.0, np.abs(a - b))
+    with np.errstate(invalid="ignore"):  # inf - inf where both_inf (masked out) or a mutant
+        err = np.where(both_inf, 0.0, np.abs(a - b))
     assert np.all(np.isfinite(err)), f"{what}: non-finite error"
     m = float(err.max()) if err.size else 0.0
     assert m <= tol, f"{what}: max err {m} > {tol}"
