@@ -12,8 +12,18 @@ Citations for each function are in ``oracle.c``. Summary:
   * ``prefill`` / ``decode``: S = Q K^T * scale, mask -> -inf, two-pass row softmax, O = P V,
     LSE = m + log l ("Attention three-op fusion", xdnf.cn/news/349386, sections 1.1, 3.2, 4.3;
     "CS336 Lecture 6", semidirectx.com, section 6; "triton-optimization" skill, section 3.5).
+  * ``chunk``: Sq new queries against a cache, query i at position L_b - Sq + i ("Hand-written
+    Triton decoder", m.nlpx.cn/news/28229, section 1.4; "Attention three-op fusion", section 4.3).
+  * ``prefill_varlen``: a padded batch, padding rows see no key ("Attention three-op fusion",
+    section 4.3).
+  * ``rope`` / ``decode_rope``: rotate-half RoPE with cos/sin tables, the new key stored in the
+    cache before attention ("triton-optimization" skill, section 3.4; "Hand-written Triton
+    decoder", sections 1.2 and 2.2).
   * ``row_partial`` / ``merge`` / ``online_row``: the online-softmax recurrence and the merge
     of key-block partials ("Attention three-op fusion", sections 2.2, 2.3 and 4.4).
+Every function is pinned to values the pages or the mathematics fix (tests/oracle_pins.py:
+closed forms, brute force on tiny inputs, reductions of chunk and varlen to prefill and
+decode, RoPE closed forms and composition, order-free merging).
 """
 from __future__ import annotations
 
